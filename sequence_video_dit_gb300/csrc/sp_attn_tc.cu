@@ -1,0 +1,835 @@
+// Tensor-core flash attention for sm_103a: tcgen05.mma with TMEM accumulators,
+// operands staged by TMA, online softmax, key masking and the pad-row rule
+// fused in; one launch covers every virtual rank x batch x local head x query
+// tile.
+//
+// Source: "LTX-2 序列并行拆解", section 换头 (after send_recv_heads each rank
+// holds all tokens x H/W heads and computes attention on them in place) and
+// section 补齐 (key-only padding mask / extended user mask; pad query rows see
+// the valid keys).  The pages name no attention kernel; this design is new.
+//
+// CTA = one (rank, batch, head) and a PAIR of 128-row query tiles (Q0, Q1)
+// sharing every K/V tile, so the tensor core always has one tile's GEMMs
+// queued while the other tile's softmax runs.  320 threads, 1 CTA per SM:
+//   warps 0-3  softmax for Q0 (thread = query row, TMEM lanes 0..127)
+//   warps 4-7  softmax for Q1
+//   warp  8    TMA producer (Q once; K, V through an NS-stage ring)
+//   warp  9    TMEM allocator + single-thread MMA issuer
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
+// P (bf16) overwrites the first 64 columns of its S buffer and feeds the PV
+// GEMM straight from TMEM (A operand in TMEM, V from shared memory).
+// Per KV tile j the MMA issue order is
+//   PV0(j) QK0(j+1) PV1(j) QK1(j+1)
+// so S_i(j+1) is written only after PV_i(j) has consumed P_i(j) (tcgen05
+// operations of one thread execute in issue order), and the commit that
+// signals S_i(j+1) also proves O_i holds PV_i(j) -- the softmax warps may
+// rescale O_i right away.  Rescaling is lazy: the running max moves only when
+// a tile's max exceeds it by more than 8 (log2 units), which keeps every
+// probability <= 2^8 and makes O rescales rare.
+//
+// Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
+// SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
+// (again with a bound) and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "sp_attn.cuh"
+
+namespace sp {
+namespace tc {
+
+constexpr int kThreads = 320;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+
+template <int D>
+struct Cfg {
+    static constexpr int DB = D / 64;             // 128-byte swizzle blocks per row
+    static constexpr int TILE = 128 * D * 2;      // bytes of a 128-row bf16 tile
+    static constexpr int NS = (D == 64) ? 4 : 2;  // K/V ring depth
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = 2 * TILE;
+    static constexpr int V_OFF = K_OFF + NS * TILE;
+    static constexpr int BYTES = V_OFF + NS * TILE;
+    static constexpr int SMEM_ALLOC = BYTES + 1024;  // + slack to align the base to 1024
+};
+
+struct alignas(128) TcParams {
+    CUtensorMap tq[SP_MAX_RANKS], tk[SP_MAX_RANKS], tv[SP_MAX_RANKS], to[SP_MAX_RANKS];
+    int W, B, Tq, Tk, Hl;
+    int n_qpairs, n_kv, n_split, kv_per_split;
+    float scale_log2;
+    int mask_kind, mask_vec4;
+    const uint8_t *mask;
+    float *part_o;    // split partials [item][split][256][D]
+    float *part_lse;  // [item][split][256], log2 domain
+    int *status;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bounded wait: false when this CTA has aborted or the wait timed out (which
+// aborts the CTA and records SP_ERR_TIMEOUT).
+__device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; i++)
+            if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            atomicCAS(status, 0, SP_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Drain wait (teardown after an abort): bounded, ignores the abort flag.
+__device__ __noinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint64_t *bar, const CUtensorMap *m, uint32_t dst, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
+// B K-major (b_mn = false) or MN-major (b_mn = true), shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn) {
+    return (1u << 4)                        // D format: f32
+           | (1u << 7)                      // A format: bf16
+           | (1u << 10)                     // B format: bf16
+           | ((b_mn ? 1u : 0u) << 16)       // B major-ness
+           | ((uint32_t)(N >> 3) << 17)     // N / 8
+           | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// TMEM loads/stores; the load wrappers include the wait so the compiler never
+// reads the destination registers early.
+__device__ __forceinline__ void tmem_ld_x128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n"
+        :
+        : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+        :
+        : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t nibble_of(uint32_t v) {
+    return ((v & 0x000000ffu) ? 1u : 0u) | ((v & 0x0000ff00u) ? 2u : 0u) | ((v & 0x00ff0000u) ? 4u : 0u) |
+           ((v & 0xff000000u) ? 8u : 0u);
+}
+// Visibility bits of keys [k, k+4) of one mask row (bounds-checked).
+__device__ __forceinline__ uint32_t mask_nibble(const uint8_t *row, int k, int Tk, bool vec4) {
+    if (vec4 && k + 3 < Tk) return nibble_of(*reinterpret_cast<const uint32_t *>(row + k));
+    uint32_t n = 0;
+#pragma unroll
+    for (int e = 0; e < 4; e++)
+        if (k + e < Tk && row[k + e]) n |= 1u << e;
+    return n;
+}
+
+// 128 visibility bits (4 words) of keys [key0, key0+128) for this thread's row.
+__device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, int key0, int lane,
+                                           uint32_t w[4]) {
+    if (p.mask_kind == SP_MASK_KEY) {
+        // warp-cooperative: lane covers keys key0 + 4*lane .. +3
+        const uint32_t nib = mask_nibble(p.mask, key0 + 4 * lane, p.Tk, p.mask_vec4);
+        uint32_t word = nib << (4 * (lane & 7));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        w[0] = __shfl_sync(0xffffffffu, word, 0);
+        w[1] = __shfl_sync(0xffffffffu, word, 8);
+        w[2] = __shfl_sync(0xffffffffu, word, 16);
+        w[3] = __shfl_sync(0xffffffffu, word, 24);
+        return;
+    }
+    if (p.mask_kind == SP_MASK_FULL && q_row < p.Tq) {
+        const uint8_t *row = p.mask + ((int64_t)b * p.Tq + q_row) * p.Tk;
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int n = 0; n < 8; n++) word |= mask_nibble(row, key0 + 32 * g + 4 * n, p.Tk, p.mask_vec4) << (4 * n);
+            w[g] = word;
+        }
+        return;
+    }
+    // no mask (or a query row past Tq): keys < Tk are visible
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        const int n = p.Tk - (key0 + 32 * g);
+        w[g] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<D>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t dsm_raw[];
+    __shared__ __align__(8) uint64_t bar_q, bar_kf[NS], bar_vf[NS], bar_ke[NS], bar_ve[NS];
+    __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t raw = smem_u32(dsm_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *const sgen = dsm_raw + (sbase - raw);
+
+    // work item: blockIdx.x -> (rank, batch, head, query pair, key split), split fastest
+    int bid = blockIdx.x;
+    const int split = bid % p.n_split;
+    bid /= p.n_split;
+    const int qp = bid % p.n_qpairs;
+    bid /= p.n_qpairs;
+    const int h = bid % p.Hl;
+    bid /= p.Hl;
+    const int b = bid % p.B;
+    const int r = bid / p.B;
+    const int kv0 = split * p.kv_per_split;
+    const int kv1 = min(p.n_kv, kv0 + p.kv_per_split);
+    const int nkv = max(0, kv1 - kv0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&bar_kf[s], 1);
+            mbar_init(&bar_vf[s], 1);
+            mbar_init(&bar_ke[s], 1);
+            mbar_init(&bar_ve[s], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&bar_sf[i], 1);
+            mbar_init(&bar_pf[i], 128);
+            mbar_init(&bar_of[i], 1);
+        }
+        mbar_init(&bar_drain, 1);
+        abort_sh = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(&tmem_base_sh), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tmem_base_sh;
+    volatile int *abort_flag = &abort_sh;
+
+    if (warp == 8) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0 && nkv > 0) {
+            prefetch_tmap(&p.tq[r]);
+            prefetch_tmap(&p.tk[r]);
+            prefetch_tmap(&p.tv[r]);
+            mbar_arrive_expect_tx(&bar_q, 2 * C::TILE);
+            for (int i = 0; i < 2; i++)
+                for (int db = 0; db < C::DB; db++)
+                    tma_load_4d(&bar_q, &p.tq[r], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, h,
+                                qp * 256 + i * 128, b);
+            int nk = 0, nv = 0;  // loads issued
+            for (int jj = 0; jj < nkv; jj++) {
+                const int s = jj % NS;
+                const uint32_t ph = (uint32_t)(jj / NS) & 1u;
+                const int krow = (kv0 + jj) * 128;
+                if (jj >= NS && !wait_bounded(&bar_ke[s], ph ^ 1u, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bar_kf[s], C::TILE);
+                for (int db = 0; db < C::DB; db++)
+                    tma_load_4d(&bar_kf[s], &p.tk[r], sbase + C::K_OFF + s * C::TILE + db * 16384, db * 64, h,
+                                krow, b);
+                nk++;
+                if (jj >= NS && !wait_bounded(&bar_ve[s], ph ^ 1u, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bar_vf[s], C::TILE);
+                for (int db = 0; db < C::DB; db++)
+                    tma_load_4d(&bar_vf[s], &p.tv[r], sbase + C::V_OFF + s * C::TILE + db * 16384, db * 64, h,
+                                krow, b);
+                nv++;
+            }
+            if (*abort_flag) {
+                // drain: the newest load of every stage (older ones were consumed)
+                wait_drain(&bar_q, 0);
+                for (int s = 0; s < NS; s++) {
+                    const int lk = nk - 1 - ((nk - 1 - s) % NS + NS) % NS;  // newest jj < nk with jj % NS == s
+                    if (nk > s) wait_drain(&bar_kf[s], (uint32_t)(lk / NS) & 1u);
+                    const int lv = nv - 1 - ((nv - 1 - s) % NS + NS) % NS;
+                    if (nv > s) wait_drain(&bar_vf[s], (uint32_t)(lv / NS) & 1u);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && nkv > 0) {
+            constexpr uint32_t idesc_qk = make_idesc(128, 128, false);
+            constexpr uint32_t idesc_pv = make_idesc(128, 64, true);
+            int issued = 0;
+            auto qk = [&](int i, int s) {
+                const uint32_t qa = sbase + C::Q_OFF + i * C::TILE;
+                const uint32_t ka = sbase + C::K_OFF + s * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk++) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                    mma_ss(tbase + (uint32_t)(i * 128), make_sdesc(qa + off, 16, 1024), make_sdesc(ka + off, 16, 1024), idesc_qk,
+                           kk > 0 ? 1u : 0u);
+                }
+                issued = 1;
+            };
+            auto pv = [&](int i, int s, bool accumulate) {
+                const uint32_t va = sbase + C::V_OFF + s * C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {  // 16 keys per step
+#pragma unroll
+                    for (int db = 0; db < C::DB; db++) {
+                        // V is MN-major (d contiguous): one 64-column swizzle block per MMA,
+                        // 8-key groups 1024 bytes apart.
+                        const uint64_t bd = make_sdesc(va + db * 16384 + kk * 2048, 1024, 1024);
+                        mma_ts(tbase + 256u + (uint32_t)(i * 128 + db * 64), tbase + (uint32_t)(i * 128 + kk * 8), bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+                    }
+                }
+                issued = 1;
+            };
+            bool ok = wait_bounded(&bar_q, 0, abort_flag, p.status) &&
+                      wait_bounded(&bar_kf[0], 0, abort_flag, p.status);
+            if (ok) {
+                tc_fence_after();
+                qk(0, 0);
+                mma_commit(&bar_sf[0]);
+                qk(1, 0);
+                mma_commit(&bar_sf[1]);
+                mma_commit(&bar_ke[0]);
+            }
+            for (int jj = 0; ok && jj < nkv; jj++) {
+                const int s = jj % NS;
+                const uint32_t ph = (uint32_t)(jj / NS) & 1u;
+                const bool more = jj + 1 < nkv;
+                const int s1 = (jj + 1) % NS;
+                const uint32_t ph1 = (uint32_t)((jj + 1) / NS) & 1u;
+                if (!wait_bounded(&bar_vf[s], ph, abort_flag, p.status)) break;
+                if (!wait_bounded(&bar_pf[0], (uint32_t)jj & 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                pv(0, s, jj > 0);
+                if (more) {
+                    if (!wait_bounded(&bar_kf[s1], ph1, abort_flag, p.status)) break;
+                    tc_fence_after();
+                    qk(0, s1);
+                    mma_commit(&bar_sf[0]);
+                } else {
+                    mma_commit(&bar_of[0]);
+                }
+                if (!wait_bounded(&bar_pf[1], (uint32_t)jj & 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                pv(1, s, jj > 0);
+                mma_commit(&bar_ve[s]);
+                if (more) {
+                    qk(1, s1);
+                    mma_commit(&bar_sf[1]);
+                    mma_commit(&bar_ke[s1]);
+                } else {
+                    mma_commit(&bar_of[1]);
+                }
+            }
+            if (*abort_flag && issued) {
+                mma_commit(&bar_drain);
+                wait_drain(&bar_drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- softmax (warps 0-7)
+        const int i = warp >> 2;       // query tile of the pair
+        const int quarter = warp & 3;  // TMEM lane quarter
+        const int row = quarter * 32 + lane;
+        const int q_row = qp * 256 + i * 128 + row;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS_me = tbase + lane_off + (uint32_t)(i * 128);
+        const uint32_t tO_me = tbase + lane_off + 256u + (uint32_t)(i * 128);
+        const float c = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int jj = 0; jj < nkv; jj++) {
+            if (!wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld_x128(tS_me, sr);
+            float *s = reinterpret_cast<float *>(sr);
+            uint32_t w[4];
+            mask_words(p, b, q_row, (kv0 + jj) * 128, lane, w);
+            if ((w[0] & w[1] & w[2] & w[3]) != 0xffffffffu) {
+#pragma unroll
+                for (int e = 0; e < 128; e++)
+                    if (!((w[e >> 5] >> (e & 31)) & 1u)) s[e] = -INFINITY;
+            }
+            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+            for (int e = 4; e < 128; e += 4) {
+                m0 = fmaxf(m0, s[e]);
+                m1 = fmaxf(m1, s[e + 1]);
+                m2 = fmaxf(m2, s[e + 2]);
+                m3 = fmaxf(m3, s[e + 3]);
+            }
+            const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            float alpha = 1.f;
+            if (mt > m) {
+                if (m == -INFINITY) {
+                    m = mt;  // no probability mass so far: O is zero
+                } else if ((mt - m) * c > kRescaleThreshold) {
+                    alpha = ex2((m - mt) * c);
+                    m = mt;
+                }
+            }
+            l *= alpha;
+            const float mc = (m == -INFINITY) ? 0.f : m * c;
+            uint32_t pk[64];
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; e++) {
+                const float p0 = ex2(fmaf(s[2 * e], c, -mc));
+                const float p1 = ex2(fmaf(s[2 * e + 1], c, -mc));
+                l0 += p0;
+                l1 += p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            l += l0 + l1;
+            tmem_st_x64(tS_me, pk);  // P over the first 64 columns of S_i
+            // O_i already holds PV_i(jj-1) (see the issue order above); rescale
+            // it when the running max moved.  Warp-uniform: tcgen05.ld/st are
+            // warp-collective, rows that did not move scale by 1.
+            if (__any_sync(0xffffffffu, alpha != 1.f) && jj > 0) {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; cc++) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO_me + cc * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; e++) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st_x32(tO_me + cc * 32, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_pf[i]);
+        }
+        if (ok && !*abort_flag) {
+            bool have = true;
+            if (nkv > 0) {
+                have = wait_bounded(&bar_of[i], 0, abort_flag, p.status);
+                tc_fence_after();
+            }
+            if (have) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                if (!SPLIT) {
+                    uint8_t *tile = sgen + C::Q_OFF + i * C::TILE;
+#pragma unroll
+                    for (int db = 0; db < C::DB; db++) {
+#pragma unroll
+                        for (int half = 0; half < 2; half++) {
+                            uint32_t o[32];
+                            if (nkv > 0) {
+                                tmem_ld_x32(tO_me + db * 64 + half * 32, o);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; e++) o[e] = 0u;
+                            }
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 16; e++)
+                                pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+#pragma unroll
+                            for (int u = 0; u < 4; u++) {
+                                const int chunk = half * 4 + u;
+                                uint4 *dst = reinterpret_cast<uint4 *>(tile + db * 16384 + row * 128 +
+                                                                       ((chunk ^ (row & 7)) << 4));
+                                *dst = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + i, 128);
+                    if (quarter == 0 && lane == 0) {
+                        for (int db = 0; db < C::DB; db++)
+                            tma_store_4d(&p.to[r], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, h,
+                                         qp * 256 + i * 128, b);
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
+                } else {
+                    const int64_t item = (((int64_t)r * p.B + b) * p.Hl + h) * p.n_qpairs + qp;
+                    const int64_t prow = (item * p.n_split + split) * 256 + i * 128 + row;
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D);
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; cc++) {
+                        uint32_t o[32];
+                        if (nkv > 0) {
+                            tmem_ld_x32(tO_me + cc * 32, o);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e++) o[e] = 0u;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            dst[cc * 8 + e] =
+                                make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                            __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                    }
+                    p.part_lse[prow] = l > 0.f ? m * c + log2f(l) : -INFINITY;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tbase, 512);
+}
+
+// Merge of split-key partials: one warp per (rank, batch, head, query) row.
+struct MergeParams {
+    void *o[SP_MAX_RANKS];
+    int64_t os[3];
+    int W, B, Tq, Hl, D, n_qpairs, n_split;
+    const float *part_o, *part_lse;
+};
+
+template <int NJ>
+__global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rowid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nrows = (int64_t)a.W * a.B * a.Hl * a.Tq;
+    if (rowid >= nrows) return;
+    int64_t t = rowid;
+    const int q = (int)(t % a.Tq);
+    t /= a.Tq;
+    const int h = (int)(t % a.Hl);
+    t /= a.Hl;
+    const int b = (int)(t % a.B);
+    const int r = (int)(t / a.B);
+    const int64_t item = (((int64_t)r * a.B + b) * a.Hl + h) * a.n_qpairs + q / 256;
+    const int row = q % 256;
+    float L = -INFINITY;
+    for (int s = 0; s < a.n_split; s++) L = fmaxf(L, a.part_lse[(item * a.n_split + s) * 256 + row]);
+    float acc[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; j++) acc[j] = 0.f;
+    float wsum = 0.f;
+    if (L != -INFINITY) {
+        for (int s = 0; s < a.n_split; s++) {
+            const int64_t prow = (item * a.n_split + s) * 256 + row;
+            const float w = exp2f(a.part_lse[prow] - L);
+            wsum += w;
+#pragma unroll
+            for (int j = 0; j < NJ; j++) acc[j] = fmaf(w, a.part_o[prow * a.D + lane + 32 * j], acc[j]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *O = (__nv_bfloat16 *)a.o[r] + b * a.os[0] + (int64_t)q * a.os[1] + h * a.os[2];
+#pragma unroll
+    for (int j = 0; j < NJ; j++) O[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static int get_encode() {
+    if (g_encode) return SP_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return set_error(SP_ERR_CUDA, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    return SP_OK;
+}
+
+// 4-D map over (d, head, token, batch) with a 64 x 1 x 128 x 1 box, 128-byte swizzle.
+static int encode_map(CUtensorMap *m, const void *base, int D, int Hl, int T, int B, const int64_t st[3]) {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hl, (cuuint64_t)T, (cuuint64_t)B};
+    // strides of a size-1 dim do not matter; give them a legal value
+    int64_t hs = Hl > 1 ? st[2] : D, ts = T > 1 ? st[1] : (int64_t)Hl * hs, bs = B > 1 ? st[0] : (int64_t)T * ts;
+    cuuint64_t strides[3] = {(cuuint64_t)hs * 2, (cuuint64_t)ts * 2, (cuuint64_t)bs * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult rc = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS) return set_error(SP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)rc);
+    return SP_OK;
+}
+
+struct SplitPlan {
+    int n_qpairs, n_kv, n_split, kv_per_split;
+    size_t extra_bytes;
+};
+
+static SplitPlan plan_split(int W, int B, int Tq, int Tk, int Hl, int D, int num_sms) {
+    SplitPlan s;
+    s.n_qpairs = (Tq + 255) / 256;
+    s.n_kv = (Tk + 127) / 128;
+    const int64_t items = (int64_t)W * B * Hl * s.n_qpairs;
+    int ns = 1;
+    if (items > 0 && items < num_sms && s.n_kv >= 8) {
+        ns = (int)(num_sms / items);
+        const int cap = s.n_kv / 4;  // at least 4 key tiles per split
+        if (ns > cap) ns = cap;
+        if (ns < 1) ns = 1;
+    }
+    s.kv_per_split = s.n_kv > 0 ? (s.n_kv + ns - 1) / ns : 1;
+    s.n_split = s.n_kv > 0 ? (s.n_kv + s.kv_per_split - 1) / s.kv_per_split : 1;
+    s.extra_bytes = s.n_split > 1 ? (size_t)items * s.n_split * 256 * (size_t)(D + 1) * sizeof(float) : 0;
+    return s;
+}
+
+}  // namespace tc
+
+size_t attn_tc_extra_bytes(int W, int B, int Tq, int Tk, int Hl, int D) {
+    DeviceInfo di;
+    if (device_info(&di) != SP_OK) return 0;
+    return tc::plan_split(W, B, Tq, Tk, Hl, D, di.num_sms).extra_bytes;
+}
+
+bool attn_tc_supported(const AttnArgs &a) {
+    if (a.dtype != SP_BF16 || (a.D != 64 && a.D != 128) || a.Tq <= 0 || a.Tk <= 0) return false;
+    for (int i = 0; i < 3; i++)
+        if (((a.qs[i] | a.ks[i] | a.os[i]) * 2) % 16 != 0) return false;
+    for (int r = 0; r < a.W; r++)
+        if (((uintptr_t)a.q[r] | (uintptr_t)a.k[r] | (uintptr_t)a.v[r] | (uintptr_t)a.o[r]) & 15) return false;
+    return true;
+}
+
+template <int D, bool SPLIT>
+static int launch_tc_t(const tc::TcParams &prm, unsigned grid, cudaStream_t st) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto kern = tc::attn_tc_kernel<D, SPLIT>;
+    if (configured_dev != dev) {
+        SP_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<D>::SMEM_ALLOC));
+        configured_dev = dev;
+    }
+    kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);
+    return check_launch("sp_attention(tcgen05)");
+}
+
+int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
+    int rc = tc::get_encode();
+    if (rc) return rc;
+    DeviceInfo di;
+    rc = device_info(&di);
+    if (rc) return rc;
+    if (di.cc_major != 10) return set_error(SP_ERR_UNSUPPORTED, "tcgen05 path needs a Blackwell (sm_10x) device");
+    static thread_local tc::TcParams prm;  // 4+ KB: keep it off the stack
+    memset(&prm, 0, sizeof(prm));
+    for (int r = 0; r < a.W; r++) {
+        if ((rc = tc::encode_map(&prm.tq[r], a.q[r], a.D, a.Hl, a.Tq, a.B, a.qs))) return rc;
+        if ((rc = tc::encode_map(&prm.tk[r], a.k[r], a.D, a.Hl, a.Tk, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.tv[r], a.v[r], a.D, a.Hl, a.Tk, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.to[r], a.o[r], a.D, a.Hl, a.Tq, a.B, a.os))) return rc;
+    }
+    tc::SplitPlan sp = tc::plan_split(a.W, a.B, a.Tq, a.Tk, a.Hl, a.D, di.num_sms);
+    if (sp.n_split > 1 && (a.extra == nullptr || a.extra_bytes < sp.extra_bytes)) {
+        sp.n_split = 1;
+        sp.kv_per_split = sp.n_kv > 0 ? sp.n_kv : 1;
+        sp.extra_bytes = 0;
+    }
+    prm.W = a.W;
+    prm.B = a.B;
+    prm.Tq = a.Tq;
+    prm.Tk = a.Tk;
+    prm.Hl = a.Hl;
+    prm.n_qpairs = sp.n_qpairs;
+    prm.n_kv = sp.n_kv;
+    prm.n_split = sp.n_split;
+    prm.kv_per_split = sp.kv_per_split;
+    prm.scale_log2 = a.scale * 1.4426950408889634f;
+    prm.mask_kind = a.mask_kind;
+    prm.mask = a.mask;
+    prm.mask_vec4 = (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0) ? 1 : 0;
+    prm.status = &a.ws->status;
+    const int64_t items = (int64_t)a.W * a.B * a.Hl * sp.n_qpairs;
+    const int64_t grid = items * sp.n_split;
+    if (grid == 0) return SP_OK;
+    if (grid > 0x7fffffffll) return set_error(SP_ERR_INVALID_ARG, "sp_attention: grid too large");
+    if (sp.n_split > 1) {
+        prm.part_o = reinterpret_cast<float *>(a.extra);
+        prm.part_lse = prm.part_o + (size_t)items * sp.n_split * 256 * a.D;
+        rc = (a.D == 64) ? launch_tc_t<64, true>(prm, (unsigned)grid, st) : launch_tc_t<128, true>(prm, (unsigned)grid, st);
+        if (rc) return rc;
+        tc::MergeParams mp;
+        memset(&mp, 0, sizeof(mp));
+        for (int r = 0; r < a.W; r++) mp.o[r] = a.o[r];
+        for (int i = 0; i < 3; i++) mp.os[i] = a.os[i];
+        mp.W = a.W;
+        mp.B = a.B;
+        mp.Tq = a.Tq;
+        mp.Hl = a.Hl;
+        mp.D = a.D;
+        mp.n_qpairs = sp.n_qpairs;
+        mp.n_split = sp.n_split;
+        mp.part_o = prm.part_o;
+        mp.part_lse = prm.part_lse;
+        const int64_t rows = (int64_t)a.W * a.B * a.Hl * a.Tq;
+        const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
+        if (a.D == 64) tc::attn_merge_kernel<2><<<blocks, 256, 0, st>>>(mp);
+        else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);
+        return check_launch("sp_attention(merge)");
+    }
+    return (a.D == 64) ? launch_tc_t<64, false>(prm, (unsigned)grid, st) : launch_tc_t<128, false>(prm, (unsigned)grid, st);
+}
+
+}  // namespace sp

@@ -1,0 +1,161 @@
+"""One sequence-parallel attention step on preallocated buffers.
+
+The call sequence follows "LTX-2 序列并行拆解" (LTX-2 sequence-parallel
+breakdown), sections 补齐 -> 切分 -> 换头 -> 还原:
+
+  self-attention                        cross-attention (small query modality)
+  1 sp_pad(Q,K,V), sp_pad_mask          1 sp_pad(K,V), sp_pad_mask (key mask)
+  2 sp_tile(Q,K,V)                      2 sp_tile(K,V)
+  3 sp_send_recv_heads(Q,K,V)           3 sp_send_recv_heads(K,V)  (Q is sliced
+                                          per rank in place: no exchange)
+  4 sp_attention on the local heads     4 sp_attention, each rank writing its
+                                          heads of the [B,Tq,H,D] output
+  5 sp_gather_heads(O)
+  6 sp_gather_output(O) cropped to the caller's length T (each rank's real
+    token count), which is the unpad
+
+Each virtual rank owns separate device allocations.  sp_pad is skipped when T
+is already a multiple of W (padding is then the identity).  Host code here
+only allocates buffers and issues library calls on the current stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (SP_MASK_FULL, SP_MASK_KEY, new_workspace, sp_attention, sp_attention_workspace_bytes,
+               sp_gather_heads, sp_gather_output, sp_pad, sp_pad_mask, sp_padded_len, sp_partition,
+               sp_send_recv_heads, sp_tile, SPValueError)
+
+
+class _NullTimer:
+    def __call__(self, name):
+        return self
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+class StageTimer:
+    """Records CUDA events around named stages on the current stream."""
+
+    def __init__(self):
+        self.events = {}
+
+    def __call__(self, name):
+        self._name = name
+        return self
+
+    def __enter__(self):
+        s = torch.cuda.Event(enable_timing=True)
+        s.record()
+        self._start = s
+        return self
+
+    def __exit__(self, *a):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        self.events.setdefault(self._name, []).append((self._start, e))
+        return False
+
+    def totals_ms(self):
+        return {k: sum(s.elapsed_time(e) for s, e in v) for k, v in self.events.items()}
+
+    def counts(self):
+        return {k: len(v) for k, v in self.events.items()}
+
+
+class SPStep:
+    """Buffers and call sequence of one SP attention step.
+
+    Self-attention: ``Tq=None``, inputs q/k/v [B,T,H,D].
+    Cross-attention: ``Tq`` query tokens (replicated on every rank), q
+    [B,Tq,H,D]; k/v [B,T,H,D] go through the exchange.
+    ``mask``: "key" (key-only padding mask) or "user" ((B,T,T) user mask,
+    self-attention only).
+    """
+
+    def __init__(self, W: int, B: int, T: int, H: int, D: int, dtype=torch.bfloat16, mask: str = "key",
+                 Tq: int | None = None, device=None):
+        if H % W:
+            raise SPValueError(2, f"H={H} is not divisible by W={W}")
+        if mask not in ("key", "user"):
+            raise SPValueError(3, f"mask must be 'key' or 'user', got {mask!r}")
+        if Tq is not None and mask == "user":
+            raise SPValueError(3, "cross-attention takes the key-only mask")
+        dev = torch.device(device or "cuda")
+        self.W, self.B, self.T, self.H, self.D, self.dtype = W, B, T, H, D, dtype
+        self.cross = Tq is not None
+        self.Tq = Tq if self.cross else None
+        self.mask_kind = mask
+        self.T_pad = sp_padded_len(T, W)
+        sp_partition(self.T_pad, W)
+        self.Tl = self.T_pad // W
+        self.Hl = H // W
+        self.need_pad = self.T_pad != T
+        names = ("k", "v") if self.cross else ("q", "k", "v")
+        self.names = names
+        emp = lambda *shape: torch.empty(*shape, dtype=dtype, device=dev)  # noqa: E731
+        self.xpad = {n: emp(B, self.T_pad, H, D) for n in names} if self.need_pad else {}
+        self.shards = {n: [emp(B, self.Tl, H, D) for _ in range(W)] for n in names}
+        self.heads = {n: [emp(B, self.T_pad, self.Hl, D) for _ in range(W)] for n in names}
+        if not self.cross:
+            self.o_heads = [emp(B, self.T_pad, self.Hl, D) for _ in range(W)]
+            self.o_shards = [emp(B, self.Tl, H, D) for _ in range(W)]
+            self.out = emp(B, T, H, D)
+            Tq_att = self.T_pad
+        else:
+            self.out = emp(B, Tq, H, D)
+            Tq_att = Tq
+        if mask == "key":
+            self.mask = torch.empty(1, 1, self.T_pad, dtype=torch.uint8, device=dev)
+        else:
+            self.mask = torch.empty(B, self.T_pad, self.T_pad, dtype=torch.uint8, device=dev)
+        self.ws_exchange = new_workspace(device=dev)
+        self.ws_attn = new_workspace(sp_attention_workspace_bytes(W, B, Tq_att, self.T_pad, self.Hl, D, dtype), dev)
+
+    # bytes each exchange launch reads + writes
+    def exchange_bytes_per_launch(self) -> int:
+        return 2 * self.B * self.T_pad * self.H * self.D * torch.empty((), dtype=self.dtype).element_size()
+
+    def n_exchange_launches(self) -> int:
+        return len(self.names) + (0 if self.cross else 1)
+
+    def __call__(self, q, k, v, user_mask=None, timer=None):
+        t = timer or _NullTimer()
+        src = {"q": q, "k": k, "v": v}
+        with t("pad"):
+            if self.need_pad:
+                for n in self.names:
+                    sp_pad(src[n], self.xpad[n])
+            if self.mask_kind == "key":
+                sp_pad_mask(None, self.mask, self.T)
+            else:
+                if user_mask is None:
+                    raise SPValueError(3, "this step was built for a user mask")
+                sp_pad_mask(user_mask, self.mask, self.T)
+        with t("tile"):
+            for n in self.names:
+                sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
+        with t("send_recv_heads"):
+            for n in self.names:
+                sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
+        kind = SP_MASK_KEY if self.mask_kind == "key" else SP_MASK_FULL
+        mask = self.mask.view(-1) if kind == SP_MASK_KEY else self.mask
+        Hl, D = self.Hl, self.D
+        with t("attention"):
+            if not self.cross:
+                sp_attention(self.heads["q"], self.heads["k"], self.heads["v"], self.o_heads, self.ws_attn,
+                             kind, mask)
+            else:
+                qv = [q[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
+                ov = [self.out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
+                sp_attention(qv, self.heads["k"], self.heads["v"], ov, self.ws_attn, kind, mask)
+        if not self.cross:
+            with t("gather_heads"):
+                sp_gather_heads(self.o_heads, self.o_shards, self.ws_exchange)
+            with t("gather_output"):
+                sp_gather_output(self.o_shards, self.out)
+        return self.out

@@ -1,0 +1,159 @@
+"""sp_attention vs the oracle (max-abs <= 1e-4 fp32, <= 2e-2 bf16), on the
+tensor-core path (bf16, D = 64 / 128) and the CUDA-core path (fp32, other D),
+across several tiles with ragged tails, all mask kinds, the strided
+cross-attention query, the split-key pass, and the degenerate rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_video_dit_gb300 as sp
+from gpu_helpers import f32_np, max_abs, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _mk(W, B, T, Hl, D, dtype, g, scale=1.0):
+    return [(torch.randn(B, T, Hl, D, generator=g) * scale).to(dtype).cuda() for _ in range(W)]
+
+
+def _run(W, B, Tq, Tk, Hl, D, dtype, mask_kind, seed=0, key_keep=0.8, full_keep=0.3):
+    g = torch.Generator().manual_seed(seed)
+    q = _mk(W, B, Tq, Hl, D, dtype, g)
+    k = _mk(W, B, Tk, Hl, D, dtype, g)
+    v = _mk(W, B, Tk, Hl, D, dtype, g)
+    o = [torch.full((B, Tq, Hl, D), float("nan"), dtype=dtype, device="cuda") for _ in range(W)]
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = (torch.rand(Tk, generator=g) < key_keep).to(torch.uint8)
+        mask[0] = 1
+    elif mask_kind == sp.SP_MASK_FULL:
+        mask = (torch.rand(B, Tq, Tk, generator=g) < full_keep).to(torch.uint8)
+        for b in range(B):
+            n = min(Tq, Tk)
+            mask[b, torch.arange(n), torch.arange(n)] = 1
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, dtype))
+    sp.sp_attention(q, k, v, o, ws, mask_kind, None if mask is None else mask.cuda())
+    torch.cuda.synchronize()
+    st, _, _ = sp.sp_workspace_status(ws)
+    assert st == 0
+    m_np = None if mask is None else mask.numpy()
+    for r in range(W):
+        ref = oracle.attention(f32_np(q[r]), f32_np(k[r]), f32_np(v[r]), mask_kind, m_np)
+        got = f32_np(o[r])
+        assert np.isfinite(got).all()
+        err = max_abs(got, ref)
+        assert err <= tol_for(dtype), f"rank {r}: max-abs {err}"
+    return q, k, v, o, mask
+
+
+@pytest.mark.parametrize("W,B,Tq,Tk,Hl,D,mask_kind", [
+    (2, 1, 300, 300, 2, 128, sp.SP_MASK_KEY),     # 2 query pairs (last ragged), 3 key tiles (ragged)
+    (2, 2, 261, 261, 1, 64, sp.SP_MASK_FULL),     # user-mask kind, D = 64
+    (1, 1, 1000, 517, 2, 128, sp.SP_MASK_NONE),   # Tq != Tk
+    (4, 1, 128, 128, 1, 128, sp.SP_MASK_KEY),     # exactly one tile
+    (1, 1, 7, 5, 3, 64, sp.SP_MASK_NONE),         # tiny, mostly out-of-range tile
+    (1, 2, 1536, 1536, 1, 128, sp.SP_MASK_KEY),   # many key tiles -> lazy rescale path
+])
+def test_tensor_core_attention(W, B, Tq, Tk, Hl, D, mask_kind):
+    _run(W, B, Tq, Tk, Hl, D, torch.bfloat16, mask_kind)
+
+
+@pytest.mark.parametrize("W,B,Tq,Tk,Hl,D,dtype,mask_kind", [
+    (2, 1, 38, 38, 2, 32, torch.float32, sp.SP_MASK_KEY),   # c1 shape
+    (1, 2, 50, 70, 2, 96, torch.bfloat16, sp.SP_MASK_FULL),  # D without a tensor-core kernel
+    (2, 1, 33, 40, 1, 256, torch.float32, sp.SP_MASK_NONE),
+])
+def test_cuda_core_attention(W, B, Tq, Tk, Hl, D, dtype, mask_kind):
+    _run(W, B, Tq, Tk, Hl, D, dtype, mask_kind)
+
+
+def test_large_logits_rescale():
+    # Scores spread over a wide range force the running max to move by more
+    # than the lazy-rescale threshold many times.
+    W, B, T, Hl, D = 1, 1, 1024, 1, 128
+    g = torch.Generator().manual_seed(3)
+    q = [(torch.randn(B, T, Hl, D, generator=g) * 3).bfloat16().cuda()]
+    k = [(torch.randn(B, T, Hl, D, generator=g) * torch.linspace(0.1, 3, T).view(1, T, 1, 1)).bfloat16().cuda()]
+    v = [torch.randn(B, T, Hl, D, generator=g).bfloat16().cuda()]
+    o = [torch.empty_like(q[0])]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16))
+    sp.sp_attention(q, k, v, o, ws)
+    ref = oracle.attention(f32_np(q[0]), f32_np(k[0]), f32_np(v[0]))
+    assert max_abs(f32_np(o[0]), ref) <= 2e-2
+
+
+def test_fully_masked_rows_are_zero():
+    W, B, T, Hl, D = 1, 1, 200, 2, 128
+    g = torch.Generator().manual_seed(4)
+    q, k, v = (_mk(W, B, T, Hl, D, torch.bfloat16, g) for _ in range(3))
+    mask = (torch.rand(B, T, T, generator=g) < 0.5).to(torch.uint8)
+    mask[0, 5] = 0
+    mask[0, 150] = 0
+    o = [torch.full_like(q[0], float("nan"))]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16))
+    sp.sp_attention(q, k, v, o, ws, sp.SP_MASK_FULL, mask.cuda())
+    got = f32_np(o[0])
+    assert (got[0, 5] == 0).all() and (got[0, 150] == 0).all()
+    ref = oracle.attention(f32_np(q[0]), f32_np(k[0]), f32_np(v[0]), oracle.MASK_FULL, mask.numpy())
+    assert max_abs(got, ref) <= 2e-2
+
+
+@pytest.mark.parametrize("Tq,Tk,H,W", [(250, 3000, 8, 2), (250, 24576 + 5, 32, 8), (17, 900, 4, 4)])
+def test_cross_attention_strided_query_and_split(Tq, Tk, H, W):
+    # The small query modality stays whole on every rank; rank r reads heads
+    # [r*Hl, (r+1)*Hl) in place and writes them into the shared output.
+    B, D = 1, 128
+    Hl = H // W
+    g = torch.Generator().manual_seed(Tq + Tk)
+    Q = torch.randn(B, Tq, H, D, generator=g).bfloat16().cuda()
+    k = _mk(W, B, Tk, Hl, D, torch.bfloat16, g)
+    v = _mk(W, B, Tk, Hl, D, torch.bfloat16, g)
+    key = torch.ones(Tk, dtype=torch.uint8)
+    key[-5:] = 0  # a key padding tail
+    out = torch.full((B, Tq, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qv = [Q[:, :, r * Hl:(r + 1) * Hl] for r in range(W)]
+    ov = [out[:, :, r * Hl:(r + 1) * Hl] for r in range(W)]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    sp.sp_attention(qv, k, v, ov, ws, sp.SP_MASK_KEY, key.cuda())
+    got = f32_np(out)
+    Qn = f32_np(Q)
+    for r in range(W):
+        ref = oracle.attention(np.ascontiguousarray(Qn[:, :, r * Hl:(r + 1) * Hl]), f32_np(k[r]), f32_np(v[r]),
+                               oracle.MASK_KEY, key.numpy())
+        assert max_abs(got[:, :, r * Hl:(r + 1) * Hl], ref) <= 2e-2
+
+
+def test_split_and_unsplit_agree():
+    # Same problem with and without the split-key workspace: both within tolerance.
+    W, B, Tq, Tk, Hl, D = 2, 1, 250, 4096, 2, 128
+    g = torch.Generator().manual_seed(9)
+    q, k, v = _mk(W, B, Tq, Hl, D, torch.bfloat16, g), _mk(W, B, Tk, Hl, D, torch.bfloat16, g), \
+        _mk(W, B, Tk, Hl, D, torch.bfloat16, g)
+    o1 = [torch.empty_like(x) for x in q]
+    o2 = [torch.empty_like(x) for x in q]
+    need = sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16)
+    assert need > sp.SP_WORKSPACE_HEADER_BYTES  # this shape splits the keys
+    sp.sp_attention(q, k, v, o1, sp.new_workspace(need))
+    sp.sp_attention(q, k, v, o2, sp.new_workspace())  # header only: no split
+    for r in range(W):
+        ref = oracle.attention(f32_np(q[r]), f32_np(k[r]), f32_np(v[r]))
+        assert max_abs(f32_np(o1[r]), ref) <= 2e-2
+        assert max_abs(f32_np(o2[r]), ref) <= 2e-2
+
+
+def test_empty_keys_give_zero():
+    W, B, Tq, Hl, D = 1, 1, 10, 1, 128
+    q = [torch.randn(B, Tq, Hl, D, device="cuda").bfloat16()]
+    k = [torch.empty(B, 0, Hl, D, dtype=torch.bfloat16, device="cuda")]
+    o = [torch.full_like(q[0], float("nan"))]
+    sp.sp_attention(q, k, k, o, sp.new_workspace())
+    assert (o[0].float() == 0).all()
+
+
+def test_attention_argument_errors():
+    q = [torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16, device="cuda")]
+    with pytest.raises(ValueError):
+        sp.sp_attention(q, q, q, q, sp.new_workspace(), sp.SP_MASK_KEY, None)
+    with pytest.raises(ValueError):
+        sp.sp_attention(q * 9, q * 9, q * 9, q * 9, sp.new_workspace())  # W = 9 > SP_MAX_RANKS

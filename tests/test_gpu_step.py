@@ -1,0 +1,116 @@
+"""The whole sequence-parallel step (pad -> tile -> send_recv_heads ->
+attention -> gather_heads -> gather_output) on the five workloads at their
+full sizes, through the C ABI, against the oracle: every output row for the
+small workloads, a strided sample of rows (exact per row: rows are
+independent) for the large ones.  Plus the correctness paragraph's claim in
+its strongest form: the sharded run equals the same kernels on the unpadded,
+unsharded tensors bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_video_dit_gb300 as sp
+import workloads
+from gpu_helpers import f32_np, max_abs, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(wl):
+    inp = workloads.make_inputs(wl)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    um = inp["user_mask"]
+    return inp, dev, (um.cuda() if um is not None else None)
+
+
+def _sample_rows(B, Tq, H, n, seed):
+    rng = np.random.default_rng(seed)
+    qs = np.unique(np.concatenate([[0, Tq - 1], rng.integers(0, Tq, n)]))
+    rows = [(b, int(q), int(rng.integers(0, H))) for b in range(B) for q in qs]
+    rows += [(0, int(Tq - 1), h) for h in range(H)] + [(B - 1, 0, h) for h in range(H)]
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_step_small_workloads_every_row(name):
+    wl = workloads.get(name)
+    inp, dev, um = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask)
+    out = f32_np(step(dev["q"], dev["k"], dev["v"], user_mask=um))
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    assert sp.sp_workspace_status(step.ws_attn)[0] == 0
+    q, k, v = (inp[n].float().numpy() for n in ("q", "k", "v"))
+    if um is None:
+        ref = oracle.attention(q, k, v)
+    else:
+        ref = oracle.attention(q, k, v, oracle.MASK_FULL, inp["user_mask"].numpy())
+    assert out.shape == ref.shape
+    assert max_abs(out, ref) <= tol_for(wl.torch_dtype)
+    # the device mask equals the oracle's extension of the user mask
+    if um is not None:
+        assert np.array_equal(step.mask.cpu().numpy(),
+                              oracle.pad_mask_user(inp["user_mask"].numpy(), step.T_pad))
+
+
+@pytest.mark.parametrize("name,nsample", [("c3", 512), ("c4", 256), ("c5", 192)])
+def test_step_large_workloads_sampled_rows(name, nsample):
+    wl = workloads.get(name)
+    inp, dev, _ = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq)
+    out = f32_np(step(dev["q"], dev["k"], dev["v"]))
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    assert sp.sp_workspace_status(step.ws_attn)[0] == 0
+    assert np.isfinite(out).all()
+    rows = _sample_rows(wl.B, wl.q_len, wl.H, nsample, wl.seed)
+    q, k, v = (inp[n].float().numpy() for n in ("q", "k", "v"))
+    ref = oracle.attention_rows(q, k, v, rows)
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert max_abs(got, ref) <= tol_for(wl.torch_dtype)
+
+
+@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
+def test_sharded_equals_unsharded_bitwise(name):
+    # Same kernels on the original tensors, one rank, every head, no padding:
+    # key tiles start at 0 in both runs and masked keys get p = 0 exactly, so
+    # every floating-point operation is the same.
+    wl = workloads.get(name)
+    inp, dev, um = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask)
+    out_sp = step(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    out_1 = torch.empty_like(out_sp)
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(1, wl.B, wl.T, wl.T, wl.H, wl.D, wl.torch_dtype))
+    if um is None:
+        sp.sp_attention([dev["q"]], [dev["k"]], [dev["v"]], [out_1], ws)
+    else:
+        sp.sp_attention([dev["q"]], [dev["k"]], [dev["v"]], [out_1], ws, sp.SP_MASK_FULL, um)
+    torch.cuda.synchronize()
+    assert torch.equal(out_sp.view(torch.int16), out_1.view(torch.int16))
+
+
+def test_pad_query_rows_are_finite_and_match_the_mean_of_v():
+    # Pad rows have a zero query and see every real key, so their output is
+    # the mean of V over the real keys (closed form).
+    wl = workloads.get("c3")
+    inp, dev, _ = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask)
+    step(dev["q"], dev["k"], dev["v"])
+    torch.cuda.synchronize()
+    vbar = inp["v"].double().mean(dim=1).numpy()  # [B,H,D]
+    Hl = step.Hl
+    for r in range(wl.W):
+        pad_rows = f32_np(step.o_heads[r][:, wl.T:])  # [B, T_pad-T, Hl, D]
+        assert np.isfinite(pad_rows).all()
+        for t in range(pad_rows.shape[1]):
+            assert max_abs(pad_rows[:, t], vbar[:, r * Hl:(r + 1) * Hl]) <= 2e-2
+
+
+def test_step_is_repeatable():
+    wl = workloads.get("c2")
+    _, dev, um = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask)
+    a = step(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    b = step(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
