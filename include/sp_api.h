@@ -157,6 +157,31 @@ SP_API int sp_send_recv_heads(const void *const *shards, void *const *heads, int
 SP_API int sp_gather_heads(const void *const *heads, void *const *shards, int W, int B, int Tl, int H,
                     int D, int elt_bytes, void *workspace, sp_stream_t stream);
 
+/* sp_send_recv_heads without a caller workspace, for callers that cannot
+ * allocate device memory: for example a plugin that is handed tensors by a
+ * host framework whose allocator it cannot reach, or an inference loop that
+ * must run inside a fixed, preallocated memory budget.  The paper has no
+ * counterpart: this is a convenience of this library.
+ *
+ * Same arguments, layout and result as sp_send_recv_heads.  The exchange's
+ * scratch (status word, finish ticket and the per-destination completion
+ * counters, SP_WORKSPACE_HEADER_BYTES = 256 bytes) lives in one static device
+ * array inside the library; every GPU that loads the library holds those 256
+ * bytes until the process exits.  The array covers at most SP_MAX_RANKS
+ * destination ranks: W > SP_MAX_RANKS is rejected with SP_ERR_INVALID_ARG.
+ * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress), so make the first call on each device before
+ * any stream capture begins.  Each call clears the counters on `stream`
+ * before its kernel runs.  All calls share the one array: calls that overlap
+ * on the GPU (other streams, other host threads) race on it; serialise them.
+ * status_out (host, may be NULL): when given, the call waits for `stream`,
+ * stores the device status of this exchange (SP_OK or SP_ERR_BARRIER) there
+ * and resets it; when NULL the call stays asynchronous. */
+SP_API int sp_send_recv_heads_noalloc(const void *const *shards, void *const *heads, int W, int B, int Tl,
+                                      int H, int D, int elt_bytes, int *status_out, sp_stream_t stream);
+
 /* Reads the workspace header (synchronises `stream`).  *status gets the
  * sticky device status (SP_OK or the first device error since the last
  * clear); counts (may be NULL) gets the per-destination CTA counts the last
@@ -174,7 +199,7 @@ SP_API int sp_sm_rotation_counts(int n_ctas, int W, int *counts);
 SP_API int sp_exchange_grid(int *n_ctas);
 
 /* ----------------------------------------------------------------------
- * Attention on the local heads ("就地算注意力").  For each rank r, batch b,
+ * Attention on the local heads (section 换头).  For each rank r, batch b,
  * local head h and query q:
  *   s_k   = scale * sum_d Q_r[b,q,h,d] * K_r[b,k,h,d]     over visible keys k
  *   O_r[b,q,h,:] = sum_k softmax(s)_k * V_r[b,k,h,:]

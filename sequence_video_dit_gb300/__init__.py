@@ -28,7 +28,7 @@ from ._lib import (SP_BF16, SP_F32, SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_
 
 __all__ = [
     "sp_padded_len", "sp_partition", "sp_pad", "sp_pad_mask", "sp_tile", "sp_send_recv_heads",
-    "sp_gather_heads", "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
+    "sp_gather_heads", "sp_send_recv_heads_noalloc", "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
     "sp_workspace_status", "sp_sm_rotation_counts", "sp_exchange_grid", "new_workspace", "SPError",
     "SPValueError", "SPStep", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
 ]
@@ -123,6 +123,21 @@ def sp_send_recv_heads(shards, heads, workspace: torch.Tensor, stream=None):
     check(lib().sp_send_recv_heads(ptr_array(shards), ptr_array(heads), W, B, Tl, H, D,
                                    shards[0].element_size(), workspace.data_ptr(), stream_handle(stream)))
     return heads
+
+
+def sp_send_recv_heads_noalloc(shards, heads, stream=None, read_status: bool = True):
+    """sp_send_recv_heads with the library's static scratch instead of a
+    caller workspace (for callers that cannot allocate device memory).
+    With read_status the call waits for the stream and returns the exchange's
+    device status (0 = OK); otherwise it stays asynchronous and returns None."""
+    _need_cuda(*shards, *heads)
+    W = len(shards)
+    B, Tl, H, D = shards[0].shape
+    st = ctypes.c_int(-1)
+    check(lib().sp_send_recv_heads_noalloc(ptr_array(shards), ptr_array(heads), W, B, Tl, H, D,
+                                           shards[0].element_size(), ctypes.byref(st) if read_status else None,
+                                           stream_handle(stream)))
+    return st.value if read_status else None
 
 
 def sp_gather_heads(heads, shards, workspace: torch.Tensor, stream=None):

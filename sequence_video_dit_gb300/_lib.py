@@ -48,6 +48,7 @@ SIGNATURES = {
     "sp_tile": (_I, [_P, _PP, _I, _I, _I, _I64, _P]),
     "sp_send_recv_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_gather_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "sp_send_recv_heads_noalloc": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _IP, _P]),
     "sp_workspace_status": (_I, [_P, _IP, _IP, _IP, _I, _P]),
     "sp_sm_rotation_counts": (_I, [_I, _I, _IP]),
     "sp_exchange_grid": (_I, [_IP]),

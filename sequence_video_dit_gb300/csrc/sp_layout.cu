@@ -14,6 +14,8 @@
 #include <stdarg.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "sp_internal.cuh"
 
 namespace sp {
@@ -295,6 +297,35 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
     return check_launch(what);
 }
 
+// ---------------------------------------------------------------- allocation-free exchange
+// Scratch of sp_send_recv_heads_noalloc: one exchange header (status word,
+// finish ticket, SP_MAX_RANKS completion counters) in static device memory,
+// so callers that cannot allocate device memory still get the exchange.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SP_WORKSPACE_HEADER_BYTES];
+
+// Device address of g_noalloc_scratch per device, looked up on the first call
+// made with that device current.  In host code the symbol names a host-side
+// stand-in, never the device memory, so only this address is passed on.
+static std::mutex g_noalloc_mu;
+static void *g_noalloc_addr[64];
+
+static int noalloc_scratch(void **out) {
+    int dev = 0;
+    SP_CUDA_CHECK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_error(SP_ERR_INVALID_ARG, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return set_error(SP_ERR_CUDA, "cudaGetSymbolAddress of the exchange scratch failed: %s",
+                             cudaGetErrorString(e));
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SP_OK;
+}
+
 }  // namespace sp
 
 using namespace sp;
@@ -434,6 +465,31 @@ int sp_gather_heads(const void *const *heads, void *const *shards, int W, int B,
                     int D, int elt_bytes, void *workspace, sp_stream_t stream) {
     return launch_exchange<true>(heads, shards, W, B, Tl, H, D, elt_bytes, workspace,
                                  (cudaStream_t)stream, "sp_gather_heads");
+}
+
+int sp_send_recv_heads_noalloc(const void *const *shards, void *const *heads, int W, int B, int Tl, int H,
+                               int D, int elt_bytes, int *status_out, sp_stream_t stream) {
+    if (W < 1 || W > SP_MAX_RANKS)
+        return set_error(SP_ERR_INVALID_ARG,
+                         "sp_send_recv_heads_noalloc: W=%d, but the static scratch holds counters for at most %d ranks",
+                         W, SP_MAX_RANKS);
+    void *ws = nullptr;
+    int rc = noalloc_scratch(&ws);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    // the counters and the ticket must start at zero; the previous call's
+    // contents are still in the array
+    SP_CUDA_CHECK(cudaMemsetAsync(ws, 0, SP_WORKSPACE_HEADER_BYTES, st));
+    rc = launch_exchange<false>(shards, heads, W, B, Tl, H, D, elt_bytes, ws, st, "sp_send_recv_heads_noalloc");
+    if (rc) return rc;
+    if (status_out) {
+        int s = 0;
+        SP_CUDA_CHECK(cudaMemcpyAsync(&s, ws, sizeof(int), cudaMemcpyDeviceToHost, st));
+        SP_CUDA_CHECK(cudaStreamSynchronize(st));
+        *status_out = s;
+        SP_CUDA_CHECK(cudaMemsetAsync(ws, 0, sizeof(int), st));
+    }
+    return SP_OK;
 }
 
 int sp_workspace_status(void *workspace, int *status, int *counts, int *n_launches, int clear,
