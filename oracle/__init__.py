@@ -9,8 +9,8 @@ The arithmetic lives in ``oracle.c`` (plain C, fp64 accumulation, no fused or
 reordered loops); this module compiles it with gcc on first use and wraps it
 with numpy.  Every routine follows the LTX-2 sequence-parallel write-up
 ("LTX-2 序列并行拆解"): 补齐 (pad), 切分 (partition), 换头 (head exchange),
-还原 (restore) and the correctness paragraph ("全局注意力没有变"): the
-sharded step is an exact redistribution around ordinary softmax attention.
+还原 (restore) and the correctness paragraph that closes 还原: the sharded
+step is an exact redistribution around ordinary softmax attention.
 
 Parity status of each function is stated in its docstring; the pins are the
 ``-m "not gpu"`` tests in ``tests/test_oracle_pins.py``.

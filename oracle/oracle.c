@@ -8,8 +8,8 @@
  *
  * Source: "LTX-2 序列并行拆解: token 切分、all2all 换头与 runner 接入全链路"
  * (LTX-2 sequence-parallel breakdown), sections 补齐 (pad), 切分 (partition),
- * 换头 (head exchange), 还原 (restore), the correctness paragraph
- * ("全局注意力没有变") and the kernel paragraphs on SM rotation and the barrier.
+ * 换头 (head exchange), 还原 (restore), the correctness paragraph that closes
+ * 还原, and the kernel paragraphs on SM rotation and the barrier.
  *
  * Everything is a plain index loop.  Layout routines move raw bytes (so they
  * are exact for any element type); attention accumulates in fp64.
@@ -172,7 +172,7 @@ void oracle_sm_rotation_counts(int n_sm, int W, int *counts) {
 }
 
 /* ------------------------------------------------------------------ */
-/* Attention on the local heads ("就地算注意力"): plain softmax attention.
+/* Attention on the local heads (section 换头): plain softmax attention.
  *   s_k = scale * sum_d Q[b,q,h,d] K[b,k,h,d]  over the visible keys k,
  *   O[b,q,h,:] = sum_k exp(s_k - max s) V[b,k,h,:] / sum_k exp(s_k - max s).
  * A row with no visible key yields 0.

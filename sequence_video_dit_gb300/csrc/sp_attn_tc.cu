@@ -102,12 +102,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Bounded wait: false when this CTA has aborted or the wait timed out (which
-// aborts the CTA and records SP_ERR_TIMEOUT).
-__device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int *status) {
+// Slow path of wait_bounded: poll with a %globaltimer bound.
+__device__ __noinline__ bool wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 32; i++)
@@ -119,6 +116,13 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volati
             return false;
         }
     }
+}
+// Bounded wait: false when this CTA has aborted or the wait timed out (which
+// aborts the CTA and records SP_ERR_TIMEOUT).  The first try is inline.
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             int *status) {
+    if (mbar_try_wait(smem_u32(bar), parity)) return true;
+    return wait_slow(bar, parity, abort_flag, status);
 }
 // Drain wait (teardown after an abort): bounded, ignores the abort flag.
 __device__ __noinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
@@ -261,6 +265,11 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -316,7 +325,7 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t dsm_raw[];
@@ -501,6 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const float c = p.scale_log2;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        // Visibility bits of the tile to come are fetched while the tensor core
+        // still works on it, never between S arriving and P leaving.
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (nkv > 0) mask_words(p, b, q_row, kv0 * 128, lane, w);
         for (int jj = 0; jj < nkv; jj++) {
             if (!wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)) {
                 ok = false;
@@ -510,22 +523,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             uint32_t sr[128];
             tmem_ld_x128(tS_me, sr);
             float *s = reinterpret_cast<float *>(sr);
-            uint32_t w[4];
-            mask_words(p, b, q_row, (kv0 + jj) * 128, lane, w);
             if ((w[0] & w[1] & w[2] & w[3]) != 0xffffffffu) {
 #pragma unroll
                 for (int e = 0; e < 128; e++)
                     if (!((w[e >> 5] >> (e & 31)) & 1u)) s[e] = -INFINITY;
             }
-            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+            float m0 = fmaxf(s[0], s[1]), m1 = fmaxf(s[2], s[3]), m2 = fmaxf(s[4], s[5]), m3 = fmaxf(s[6], s[7]);
 #pragma unroll
-            for (int e = 4; e < 128; e += 4) {
-                m0 = fmaxf(m0, s[e]);
-                m1 = fmaxf(m1, s[e + 1]);
-                m2 = fmaxf(m2, s[e + 2]);
-                m3 = fmaxf(m3, s[e + 3]);
+            for (int e = 8; e < 128; e += 8) {
+                m0 = fmax3(m0, s[e], s[e + 1]);
+                m1 = fmax3(m1, s[e + 2], s[e + 3]);
+                m2 = fmax3(m2, s[e + 4], s[e + 5]);
+                m3 = fmax3(m3, s[e + 6], s[e + 7]);
             }
-            const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            const float mt = fmax3(m0, m1, fmaxf(m2, m3));
             float alpha = 1.f;
             if (mt > m) {
                 if (m == -INFINITY) {
@@ -538,16 +549,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             l *= alpha;
             const float mc = (m == -INFINITY) ? 0.f : m * c;
             uint32_t pk[64];
-            float l0 = 0.f, l1 = 0.f;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 64; e++) {
+            for (int e = 0; e < 64; e += 2) {
                 const float p0 = ex2(fmaf(s[2 * e], c, -mc));
                 const float p1 = ex2(fmaf(s[2 * e + 1], c, -mc));
+                const float p2 = ex2(fmaf(s[2 * e + 2], c, -mc));
+                const float p3 = ex2(fmaf(s[2 * e + 3], c, -mc));
                 l0 += p0;
                 l1 += p1;
+                l2 += p2;
+                l3 += p3;
                 pk[e] = pack_bf16x2(p0, p1);
+                pk[e + 1] = pack_bf16x2(p2, p3);
             }
-            l += l0 + l1;
+            l += (l0 + l1) + (l2 + l3);
             tmem_st_x64(tS_me, pk);  // P over the first 64 columns of S_i
             // O_i already holds PV_i(jj-1) (see the issue order above); rescale
             // it when the running max moved.  Warp-uniform: tcgen05.ld/st are
@@ -565,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_pf[i]);
+            if (jj + 1 < nkv) mask_words(p, b, q_row, (kv0 + jj + 1) * 128, lane, w);
         }
         if (ok && !*abort_flag) {
             bool have = true;
