@@ -325,7 +325,7 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool SPLIT>
-__global__ void __maxnreg__(200) attn_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t dsm_raw[];
