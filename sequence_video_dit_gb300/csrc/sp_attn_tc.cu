@@ -13,7 +13,8 @@
 // queued while the other tile's softmax runs.  320 threads, 1 CTA per SM:
 //   warps 0-3  softmax for Q0 (thread = query row, TMEM lanes 0..127)
 //   warps 4-7  softmax for Q1
-//   warp  8    TMA producer (Q once; K, V through an NS-stage ring)
+//   warp  8    TMA producer (Q once; K and V tiles through one shared ring of
+//              NSLOT slots, loaded in the order K0 V0 K1 V1 ...)
 //   warp  9    TMEM allocator + single-thread MMA issuer
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D).
 // P (bf16) overwrites the first 64 columns of its S buffer and feeds the PV
@@ -49,18 +50,17 @@ template <int D>
 struct Cfg {
     static constexpr int DB = D / 64;             // 128-byte swizzle blocks per row
     static constexpr int TILE = 128 * D * 2;      // bytes of a 128-row bf16 tile
-    static constexpr int NS = (D == 64) ? 4 : 2;  // K/V ring depth
+    static constexpr int NSLOT = (D == 64) ? 10 : 5;  // K/V ring slots (2.5 tiles of each ahead at D=128)
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = 2 * TILE;
-    static constexpr int V_OFF = K_OFF + NS * TILE;
-    static constexpr int BYTES = V_OFF + NS * TILE;
+    static constexpr int R_OFF = 2 * TILE;
+    static constexpr int BYTES = R_OFF + NSLOT * TILE;
     static constexpr int SMEM_ALLOC = BYTES + 1024;  // + slack to align the base to 1024
 };
 
 struct alignas(128) TcParams {
     CUtensorMap tq[SP_MAX_RANKS], tk[SP_MAX_RANKS], tv[SP_MAX_RANKS], to[SP_MAX_RANKS];
     int W, B, Tq, Tk, Hl;
-    int n_qpairs, n_kv, n_split, kv_per_split;
+    int n_qpairs, n_qp_grid, n_kv, n_split, kv_per_split;
     float scale_log2;
     int mask_kind, mask_vec4;
     const uint8_t *mask;
@@ -143,6 +143,24 @@ __device__ __forceinline__ void tma_load_4d(uint64_t *bar, const CUtensorMap *m,
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
         : "memory");
 }
+// Same copy, delivered to the same shared-memory offset of every CTA in
+// `mask` (this cluster), each of whose barriers at `bar`'s offset gets the bytes.
+__device__ __forceinline__ void tma_load_4d_mc(uint64_t *bar, const CUtensorMap *m, uint32_t dst, int c0, int c1,
+                                               int c2, int c3, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2,
                                              int c3) {
     asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
@@ -192,6 +210,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
         "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Commit whose arrival lands on the barrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -324,12 +350,16 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool SPLIT>
+// MC: the grid is made of 2-CTA clusters whose CTAs serve adjacent query pairs
+// of the same (rank, batch, head); each CTA loads one 64-column half of every
+// K/V tile and multicasts it to both, so a K/V tile leaves L2 once per four
+// query tiles instead of once per two.
+template <int D, bool SPLIT, bool MC>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
-    constexpr int NS = C::NS;
+    constexpr int NSLOT = C::NSLOT;
     extern __shared__ uint8_t dsm_raw[];
-    __shared__ __align__(8) uint64_t bar_q, bar_kf[NS], bar_vf[NS], bar_ke[NS], bar_ve[NS];
+    __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_empty[NSLOT];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -339,12 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t *const sgen = dsm_raw + (sbase - raw);
 
-    // work item: blockIdx.x -> (rank, batch, head, query pair, key split), split fastest
+    // work item: blockIdx.x -> (rank, batch, head, key split, query pair), query pair
+    // fastest; with MC, n_qp_grid rounds n_qpairs up to even and a surplus CTA
+    // (qp == n_qpairs) only helps load K/V for its cluster partner
     int bid = blockIdx.x;
+    const int qp = bid % p.n_qp_grid;
+    bid /= p.n_qp_grid;
     const int split = bid % p.n_split;
     bid /= p.n_split;
-    const int qp = bid % p.n_qpairs;
-    bid /= p.n_qpairs;
     const int h = bid % p.Hl;
     bid /= p.Hl;
     const int b = bid % p.B;
@@ -352,14 +384,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int kv0 = split * p.kv_per_split;
     const int kv1 = min(p.n_kv, kv0 + p.kv_per_split);
     const int nkv = max(0, kv1 - kv0);
+    // CTAs of one head run in step; starting each query pair at a different key
+    // tile spreads their concurrent K/V reads over L2 instead of all CTAs asking
+    // for the same tile at once.  Softmax is order-free, so only rounding moves.
+    const int rot = nkv > 0 ? (int)(((unsigned)(qp >> 1) * 7u) % (unsigned)nkv) : 0;  // same in both CTAs of a cluster
+    const uint32_t crank = MC ? cluster_ctarank() : 0u;
+    auto key_tile = [&](int jj) { int t = jj + rot; return kv0 + (t >= nkv ? t - nkv : t); };
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
-        for (int s = 0; s < NS; s++) {
-            mbar_init(&bar_kf[s], 1);
-            mbar_init(&bar_vf[s], 1);
-            mbar_init(&bar_ke[s], 1);
-            mbar_init(&bar_ve[s], 1);
+        for (int s = 0; s < NSLOT; s++) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], MC ? 2 : 1);  // with MC both CTAs must release a slot
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar_sf[i], 1);
@@ -376,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();  // the partner's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
     volatile int *abort_flag = &abort_sh;
@@ -391,32 +428,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 for (int db = 0; db < C::DB; db++)
                     tma_load_4d(&bar_q, &p.tq[r], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, h,
                                 qp * 256 + i * 128, b);
-            int nk = 0, nv = 0;  // loads issued
-            for (int jj = 0; jj < nkv; jj++) {
-                const int s = jj % NS;
-                const uint32_t ph = (uint32_t)(jj / NS) & 1u;
-                const int krow = (kv0 + jj) * 128;
-                if (jj >= NS && !wait_bounded(&bar_ke[s], ph ^ 1u, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&bar_kf[s], C::TILE);
-                for (int db = 0; db < C::DB; db++)
-                    tma_load_4d(&bar_kf[s], &p.tk[r], sbase + C::K_OFF + s * C::TILE + db * 16384, db * 64, h,
-                                krow, b);
-                nk++;
-                if (jj >= NS && !wait_bounded(&bar_ve[s], ph ^ 1u, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&bar_vf[s], C::TILE);
-                for (int db = 0; db < C::DB; db++)
-                    tma_load_4d(&bar_vf[s], &p.tv[r], sbase + C::V_OFF + s * C::TILE + db * 16384, db * 64, h,
-                                krow, b);
-                nv++;
+            // load n: K of key tile n/2 (n even) or V (n odd) into slot n % NSLOT
+            const int nloads = 2 * nkv;
+            int n = 0;
+            for (; n < nloads; n++) {
+                const int slot = n % NSLOT;
+                const int use = n / NSLOT;
+                if (use > 0 && !wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bar_full[slot], C::TILE);
+                const CUtensorMap *m = (n & 1) ? &p.tv[r] : &p.tk[r];
+                const int krow = key_tile(n >> 1) * 128;
+                if (MC) {
+                    // this CTA's half (64 columns) of the tile, written into both CTAs
+                    tma_load_4d_mc(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + crank * 16384, crank * 64, h,
+                                   krow, b, (uint16_t)0x3);
+                } else {
+                    for (int db = 0; db < C::DB; db++)
+                        tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, h,
+                                    krow, b);
+                }
             }
             if (*abort_flag) {
-                // drain: the newest load of every stage (older ones were consumed)
+                // drain: the newest load of every slot (older ones were consumed)
                 wait_drain(&bar_q, 0);
-                for (int s = 0; s < NS; s++) {
-                    const int lk = nk - 1 - ((nk - 1 - s) % NS + NS) % NS;  // newest jj < nk with jj % NS == s
-                    if (nk > s) wait_drain(&bar_kf[s], (uint32_t)(lk / NS) & 1u);
-                    const int lv = nv - 1 - ((nv - 1 - s) % NS + NS) % NS;
-                    if (nv > s) wait_drain(&bar_vf[s], (uint32_t)(lv / NS) & 1u);
+                for (int slot = 0; slot < NSLOT && slot < n; slot++) {
+                    const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
+                    wait_drain(&bar_full[slot], (uint32_t)(last / NSLOT) & 1u);
                 }
             }
         }
@@ -425,11 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0 && nkv > 0) {
             constexpr uint32_t idesc_qk = make_idesc(128, 128, false);
-            constexpr uint32_t idesc_pv = make_idesc(128, 64, true);
+            constexpr uint32_t idesc_pv = make_idesc(128, D, true);
             int issued = 0;
-            auto qk = [&](int i, int s) {
+            auto qk = [&](int i, int slot) {
                 const uint32_t qa = sbase + C::Q_OFF + i * C::TILE;
-                const uint32_t ka = sbase + C::K_OFF + s * C::TILE;
+                const uint32_t ka = sbase + C::R_OFF + slot * C::TILE;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
                     const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
@@ -438,56 +475,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 }
                 issued = 1;
             };
-            auto pv = [&](int i, int s, bool accumulate) {
-                const uint32_t va = sbase + C::V_OFF + s * C::TILE;
+            auto pv = [&](int i, int slot, bool accumulate) {
+                const uint32_t va = sbase + C::R_OFF + slot * C::TILE;
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {  // 16 keys per step
-#pragma unroll
-                    for (int db = 0; db < C::DB; db++) {
-                        // V is MN-major (d contiguous): one 64-column swizzle block per MMA,
-                        // 8-key groups 1024 bytes apart.
-                        const uint64_t bd = make_sdesc(va + db * 16384 + kk * 2048, 1024, 1024);
-                        mma_ts(tbase + 256u + (uint32_t)(i * 128 + db * 64), tbase + (uint32_t)(i * 128 + kk * 8), bd, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < 8; kk++) {  // 16 keys per step, all D columns at once
+                    // V is MN-major (d contiguous): 64-column swizzle blocks 16 KB apart
+                    // (leading byte offset), 8-key groups 1024 bytes apart (stride offset).
+                    const uint64_t bd = make_sdesc(va + kk * 2048, 16384, 1024);
+                    mma_ts(tbase + 256u + (uint32_t)(i * 128), tbase + (uint32_t)(i * 128 + kk * 8), bd, idesc_pv,
+                           (accumulate || kk > 0) ? 1u : 0u);
                 }
                 issued = 1;
             };
+            // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
+            auto kslot = [](int j) { return (2 * j) % NSLOT; };
+            // a slot is free once every CTA that received the tile has consumed it
+            auto release = [&](int slot) {
+                if (MC) mma_commit_mc(&bar_empty[slot], (uint16_t)0x3);
+                else mma_commit(&bar_empty[slot]);
+            };
+            auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };
+            auto kpar = [](int j) { return (uint32_t)((2 * j) / NSLOT) & 1u; };
+            auto vpar = [](int j) { return (uint32_t)((2 * j + 1) / NSLOT) & 1u; };
             bool ok = wait_bounded(&bar_q, 0, abort_flag, p.status) &&
-                      wait_bounded(&bar_kf[0], 0, abort_flag, p.status);
+                      wait_bounded(&bar_full[kslot(0)], kpar(0), abort_flag, p.status);
             if (ok) {
                 tc_fence_after();
-                qk(0, 0);
+                qk(0, kslot(0));
                 mma_commit(&bar_sf[0]);
-                qk(1, 0);
+                qk(1, kslot(0));
                 mma_commit(&bar_sf[1]);
-                mma_commit(&bar_ke[0]);
+                release(kslot(0));
             }
             for (int jj = 0; ok && jj < nkv; jj++) {
-                const int s = jj % NS;
-                const uint32_t ph = (uint32_t)(jj / NS) & 1u;
                 const bool more = jj + 1 < nkv;
-                const int s1 = (jj + 1) % NS;
-                const uint32_t ph1 = (uint32_t)((jj + 1) / NS) & 1u;
-                if (!wait_bounded(&bar_vf[s], ph, abort_flag, p.status)) break;
+                if (!wait_bounded(&bar_full[vslot(jj)], vpar(jj), abort_flag, p.status)) break;
                 if (!wait_bounded(&bar_pf[0], (uint32_t)jj & 1u, abort_flag, p.status)) break;
                 tc_fence_after();
-                pv(0, s, jj > 0);
+                pv(0, vslot(jj), jj > 0);
                 if (more) {
-                    if (!wait_bounded(&bar_kf[s1], ph1, abort_flag, p.status)) break;
+                    if (!wait_bounded(&bar_full[kslot(jj + 1)], kpar(jj + 1), abort_flag, p.status)) break;
                     tc_fence_after();
-                    qk(0, s1);
+                    qk(0, kslot(jj + 1));
                     mma_commit(&bar_sf[0]);
                 } else {
                     mma_commit(&bar_of[0]);
                 }
                 if (!wait_bounded(&bar_pf[1], (uint32_t)jj & 1u, abort_flag, p.status)) break;
                 tc_fence_after();
-                pv(1, s, jj > 0);
-                mma_commit(&bar_ve[s]);
+                pv(1, vslot(jj), jj > 0);
+                release(vslot(jj));
                 if (more) {
-                    qk(1, s1);
+                    qk(1, kslot(jj + 1));
                     mma_commit(&bar_sf[1]);
-                    mma_commit(&bar_ke[s1]);
+                    release(kslot(jj + 1));
                 } else {
                     mma_commit(&bar_of[1]);
                 }
@@ -513,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // Visibility bits of the tile to come are fetched while the tensor core
         // still works on it, never between S arriving and P leaving.
         uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (nkv > 0) mask_words(p, b, q_row, kv0 * 128, lane, w);
+        if (nkv > 0) mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
         for (int jj = 0; jj < nkv; jj++) {
             if (!wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)) {
                 ok = false;
@@ -581,9 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_pf[i]);
-            if (jj + 1 < nkv) mask_words(p, b, q_row, (kv0 + jj + 1) * 128, lane, w);
+            if (jj + 1 < nkv) mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
         }
-        if (ok && !*abort_flag) {
+        if (ok && !*abort_flag && qp < p.n_qpairs) {
             bool have = true;
             if (nkv > 0) {
                 have = wait_bounded(&bar_of[i], 0, abort_flag, p.status);
@@ -654,6 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     if (warp == 9) tmem_dealloc(tbase, 512);
+    // the partner may still be delivering into this CTA's shared memory or
+    // barriers until it is done too
+    if (MC) cluster_sync();
 }
 
 // Merge of split-key partials: one warp per (rank, batch, head, query) row.
@@ -769,18 +813,37 @@ bool attn_tc_supported(const AttnArgs &a) {
     return true;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool MC>
 static int launch_tc_t(const tc::TcParams &prm, unsigned grid, cudaStream_t st) {
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = tc::attn_tc_kernel<D, SPLIT>;
+    auto kern = tc::attn_tc_kernel<D, SPLIT, MC>;
     if (configured_dev != dev) {
         SP_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<D>::SMEM_ALLOC));
         configured_dev = dev;
     }
-    kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);
-    return check_launch("sp_attention(tcgen05)");
+    if (!MC) {
+        kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);
+        return check_launch("sp_attention(tcgen05)");
+    }
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(tc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc::Cfg<D>::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
+    if (e != cudaSuccess)
+        return set_error(SP_ERR_CUDA, "sp_attention(tcgen05, cluster) launch failed: %s", cudaGetErrorString(e));
+    return check_launch("sp_attention(tcgen05, cluster)");
 }
 
 int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
@@ -809,7 +872,10 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.Tq = a.Tq;
     prm.Tk = a.Tk;
     prm.Hl = a.Hl;
+    // K/V multicast across a CTA pair pays off when a head has several query pairs
+    const bool mc = a.D == 128 && sp.n_split == 1 && sp.n_qpairs >= 2;
     prm.n_qpairs = sp.n_qpairs;
+    prm.n_qp_grid = mc ? (sp.n_qpairs + 1) & ~1 : sp.n_qpairs;
     prm.n_kv = sp.n_kv;
     prm.n_split = sp.n_split;
     prm.kv_per_split = sp.kv_per_split;
@@ -819,13 +885,14 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.mask_vec4 = (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0) ? 1 : 0;
     prm.status = &a.ws->status;
     const int64_t items = (int64_t)a.W * a.B * a.Hl * sp.n_qpairs;
-    const int64_t grid = items * sp.n_split;
+    const int64_t grid = (int64_t)a.W * a.B * a.Hl * prm.n_qp_grid * sp.n_split;
     if (grid == 0) return SP_OK;
     if (grid > 0x7fffffffll) return set_error(SP_ERR_INVALID_ARG, "sp_attention: grid too large");
     if (sp.n_split > 1) {
         prm.part_o = reinterpret_cast<float *>(a.extra);
         prm.part_lse = prm.part_o + (size_t)items * sp.n_split * 256 * a.D;
-        rc = (a.D == 64) ? launch_tc_t<64, true>(prm, (unsigned)grid, st) : launch_tc_t<128, true>(prm, (unsigned)grid, st);
+        rc = (a.D == 64) ? launch_tc_t<64, true, false>(prm, (unsigned)grid, st)
+                         : launch_tc_t<128, true, false>(prm, (unsigned)grid, st);
         if (rc) return rc;
         tc::MergeParams mp;
         memset(&mp, 0, sizeof(mp));
@@ -846,7 +913,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);
         return check_launch("sp_attention(merge)");
     }
-    return (a.D == 64) ? launch_tc_t<64, false>(prm, (unsigned)grid, st) : launch_tc_t<128, false>(prm, (unsigned)grid, st);
+    if (a.D == 64) return launch_tc_t<64, false, false>(prm, (unsigned)grid, st);
+    return mc ? launch_tc_t<128, false, true>(prm, (unsigned)grid, st) : launch_tc_t<128, false, false>(prm, (unsigned)grid, st);
 }
 
 }  // namespace sp
