@@ -464,27 +464,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             constexpr uint32_t idesc_qk = make_idesc(128, 128, false);
             constexpr uint32_t idesc_pv = make_idesc(128, D, true);
             int issued = 0;
+            // Descriptors are built once; a K step or a ring slot only moves the
+            // 14-bit start-address field (shared-memory offsets are < 2^18, so the
+            // field never carries into the next one).
+            const uint64_t dq0 = make_sdesc(sbase + C::Q_OFF, 16, 1024);
+            const uint64_t dq1 = make_sdesc(sbase + C::Q_OFF + C::TILE, 16, 1024);
+            const uint64_t dk0 = make_sdesc(sbase + C::R_OFF, 16, 1024);     // K tile: K-major
+            const uint64_t dv0 = make_sdesc(sbase + C::R_OFF, 16384, 1024);  // V tile: MN-major
+            constexpr uint32_t kSlotStep = C::TILE >> 4;
             auto qk = [&](int i, int slot) {
-                const uint32_t qa = sbase + C::Q_OFF + i * C::TILE;
-                const uint32_t ka = sbase + C::R_OFF + slot * C::TILE;
+                const uint64_t a = i ? dq1 : dq0;
+                const uint64_t bk = dk0 + (uint64_t)(slot * kSlotStep);
+                const uint32_t d = tbase + (uint32_t)(i * 128);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk++) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
-                    mma_ss(tbase + (uint32_t)(i * 128), make_sdesc(qa + off, 16, 1024), make_sdesc(ka + off, 16, 1024), idesc_qk,
-                           kk > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);  // (kk/4)*16 KB + (kk%4)*32 B
+                    mma_ss(d, a + off, bk + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 issued = 1;
             };
             auto pv = [&](int i, int slot, bool accumulate) {
-                const uint32_t va = sbase + C::R_OFF + slot * C::TILE;
+                // V is MN-major (d contiguous): 64-column swizzle blocks 16 KB apart
+                // (leading byte offset), 8-key groups 1024 bytes apart (stride offset).
+                const uint64_t bv = dv0 + (uint64_t)(slot * kSlotStep);
+                const uint32_t d = tbase + 256u + (uint32_t)(i * 128);
+                const uint32_t pa = tbase + (uint32_t)(i * 128);
 #pragma unroll
-                for (int kk = 0; kk < 8; kk++) {  // 16 keys per step, all D columns at once
-                    // V is MN-major (d contiguous): 64-column swizzle blocks 16 KB apart
-                    // (leading byte offset), 8-key groups 1024 bytes apart (stride offset).
-                    const uint64_t bd = make_sdesc(va + kk * 2048, 16384, 1024);
-                    mma_ts(tbase + 256u + (uint32_t)(i * 128), tbase + (uint32_t)(i * 128 + kk * 8), bd, idesc_pv,
-                           (accumulate || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; kk++)  // 16 keys (2048 bytes of V) per step, all D columns at once
+                    mma_ts(d, pa + (uint32_t)(kk * 8), bv + (uint64_t)(kk * 128), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
                 issued = 1;
             };
             // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
