@@ -156,6 +156,22 @@ def weak_scaling_value(flops_per_rank: float, world: int, seconds_max: float) ->
     return flops_per_rank * world / seconds_max / 1e12
 
 
+def workload_config(wl, world: int, big_inputs: bool) -> dict:
+    return {
+        "workload": f"{wl.name}: W={wl.W} virtual ranks, B={wl.B}, "
+                    + (f"Tq={wl.Tq}, Tk={wl.T}" if wl.cross else f"T={wl.T}")
+                    + f", H={wl.H}, D={wl.D}, {wl.dtype}, {wl.mask} mask",
+        "W": wl.W, "B": wl.B, "T": wl.T, "Tq": wl.q_len, "H": wl.H, "D": wl.D,
+        "parallelism": f"sp{wl.W} virtual ranks on 1 GPU" + (f", x{world} independent replicas" if world > 1 else ""),
+        "l2": "inputs larger than L2" if big_inputs else f"L2 flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+    }
+
+
+def inputs_exceed_l2(wl) -> bool:
+    in_bytes = (wl.q_len + 2 * wl.T) * wl.B * wl.H * wl.D * wl.elt
+    return in_bytes > 2 * L2_FLUSH_BYTES
+
+
 # ---------------------------------------------------------------- CPU oracle
 def oracle_sample_tflops(wl, budget_s: float, threads: int, seed: int = 0):
     """Oracle attention on a bounded random sample of output rows of the
@@ -201,7 +217,7 @@ def run_ours(args, world, rank, local):
     out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     in_bytes = sum(t.numel() * t.element_size() for t in d_in.values())
-    big_inputs = in_bytes > 2 * (flush.numel())
+    big_inputs = inputs_exceed_l2(wl)
     flops = wl.flops()
 
     def one(timer=None):
@@ -284,14 +300,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) inputs shaped like the workload; no weights involved)",
-        "config": {
-            "workload": f"{wl.name}: W={wl.W} virtual ranks, B={wl.B}, "
-                        + (f"Tq={wl.Tq}, Tk={wl.T}" if wl.cross else f"T={wl.T}")
-                        + f", H={wl.H}, D={wl.D}, {wl.dtype}, {wl.mask} mask",
-            "W": wl.W, "B": wl.B, "T": wl.T, "Tq": wl.q_len, "H": wl.H, "D": wl.D,
-            "parallelism": f"sp{wl.W} virtual ranks on 1 GPU" + (f", x{world} independent replicas" if world > 1 else ""),
-            "l2": "inputs larger than L2" if big_inputs else f"L2 flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
-        },
+        "config": workload_config(wl, world, big_inputs),
         "head_exchange": {"value": round(exch_gbs, 1) if exch_gbs else None, "unit": "GB/s",
                           "launches_per_step": step.n_exchange_launches(),
                           "bytes_per_launch": step.exchange_bytes_per_launch()},
@@ -337,7 +346,7 @@ def run_reference(args, world, rank):
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
         "data": "synthetic (seeded N(0,1) inputs shaped like the workload)",
-        "config": {"workload": wl.name, "W": wl.W, "B": wl.B, "T": wl.T, "Tq": wl.q_len, "H": wl.H, "D": wl.D},
+        "config": workload_config(wl, world, inputs_exceed_l2(wl)),
         "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
