@@ -156,6 +156,22 @@ def weak_scaling_value(flops_per_rank: float, world: int, seconds_max: float) ->
     return flops_per_rank * world / seconds_max / 1e12
 
 
+def attention_traffic_bytes(name: str):
+    """DRAM bytes (read + write) per attention launch from the committed ncu
+    summary (profiles/attention_dram.md), or None when it has no row."""
+    import re
+
+    path = os.path.join(ROOT, "profiles", "attention_dram.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"\|\s*(c\d)\s*\|\s*([0-9.]+)\s*\|\s*([0-9.]+)\s*\|", line)
+            if m and m.group(1) == name:
+                return int(round((float(m.group(2)) + float(m.group(3))) * 1e6))
+    return None
+
+
 def workload_config(wl, world: int, big_inputs: bool) -> dict:
     return {
         "workload": f"{wl.name}: W={wl.W} virtual ranks, B={wl.B}, "
@@ -282,11 +298,7 @@ def run_ours(args, world, rank, local):
     peaks = load_peaks()
     achieved = flops / (attn_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
-    traffic = None
-    prof_traffic = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    if os.path.exists(prof_traffic):
-        with open(prof_traffic) as f:
-            traffic = json.load(f).get(wl.name)
+    traffic = attention_traffic_bytes(wl.name)
     result = {
         "metric": METRIC,
         "value": round(weak_scaling_value(flops, world, ms_max / 1e3), 3),

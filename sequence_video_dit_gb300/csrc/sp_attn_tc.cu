@@ -230,6 +230,17 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Named barrier that also ANDs a predicate over its participants.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -710,8 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (nkv > 0) mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
         for (int jj = 0; jj < nkv; jj++) {
-            if (!(PAIR ? wait_bounded_cl(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)
-                       : wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status))) {
+            const bool s_ok = PAIR ? wait_bounded_cl(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)
+                                   : wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, s_ok)) {  // leave together: the loop body is warp-collective
                 ok = false;
                 break;
             }
@@ -786,11 +798,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             if (jj + 1 < nkv) mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
         }
-        if (ok && !*abort_flag && qp < p.n_qpairs) {
+        // the epilogue has a 128-thread barrier: the tile's four warps decide together
+        const bool epi = named_bar_and(1 + i, 128, ok && !*abort_flag);
+        if (epi && qp < p.n_qpairs) {
             bool have = true;
             if (nkv > 0) {
                 have = PAIR ? wait_bounded_cl(&bar_of[i], 0, abort_flag, p.status)
                             : wait_bounded(&bar_of[i], 0, abort_flag, p.status);
+                have = __all_sync(0xffffffffu, have);
                 tc_fence_after();
             }
             if (have) {
@@ -1041,16 +1056,16 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.Tq = a.Tq;
     prm.Tk = a.Tk;
     prm.Hl = a.Hl;
-    // With several query pairs per head, CTA pairs share each K/V tile: MODE 2
-    // (one M=256 tensor-core pass per pair, the default) or MODE 1 (multicast
-    // loads, separate M=128 passes); SP_ATTN_CLUSTER_MODE=0/1/2 overrides it
-    // for measurements.
+    // With several query pairs per head, CTA pairs may share each K/V tile:
+    // MODE 2 (one M=256 tensor-core pass per pair) or MODE 1 (multicast loads,
+    // separate M=128 passes).  Both measure the same as MODE 0 (independent
+    // CTAs), which stays the default; SP_ATTN_CLUSTER_MODE=0/1/2 selects one.
     static const int mode_env = [] {
         const char *e = getenv("SP_ATTN_CLUSTER_MODE");
         return (e && e[0] >= '0' && e[0] <= '2' && e[1] == 0) ? e[0] - '0' : -1;
     }();
     const bool pairable = a.D == 128 && sp.n_split == 1 && sp.n_qpairs >= 2;
-    const int mode = pairable ? (mode_env >= 0 ? mode_env : 2) : 0;
+    const int mode = pairable ? (mode_env >= 0 ? mode_env : 0) : 0;
     const bool mc = mode != 0;
     prm.n_qpairs = sp.n_qpairs;
     prm.n_qp_grid = mc ? (sp.n_qpairs + 1) & ~1 : sp.n_qpairs;
