@@ -123,8 +123,14 @@ class SPStep:
     def n_exchange_launches(self) -> int:
         return len(self.names) + (0 if self.cross else 1)
 
-    def __call__(self, q, k, v, user_mask=None, timer=None):
+    def __call__(self, q, k, v, user_mask=None, timer=None, out=None):
+        """Runs the step on the current stream and returns the output tensor
+        (``out`` if given, shaped like ``self.out``, else ``self.out``)."""
         t = timer or _NullTimer()
+        if out is None:
+            out = self.out
+        elif tuple(out.shape) != tuple(self.out.shape) or out.dtype != self.out.dtype:
+            raise SPValueError(3, "out must match the step's output shape and dtype")
         src = {"q": q, "k": k, "v": v}
         with t("pad"):
             if self.need_pad:
@@ -151,11 +157,11 @@ class SPStep:
                              kind, mask)
             else:
                 qv = [q[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
-                ov = [self.out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
+                ov = [out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
                 sp_attention(qv, self.heads["k"], self.heads["v"], ov, self.ws_attn, kind, mask)
         if not self.cross:
             with t("gather_heads"):
                 sp_gather_heads(self.o_heads, self.o_shards, self.ws_exchange)
             with t("gather_output"):
-                sp_gather_output(self.o_shards, self.out)
-        return self.out
+                sp_gather_output(self.o_shards, out)
+        return out
