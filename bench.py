@@ -275,6 +275,9 @@ def run_ours(args, world, rank, local):
     x_bytes = step.exchange_bytes_per_launch() * step.n_exchange_launches() * args.steps
     exch_gbs = x_bytes / (x_ms / 1e3) / 1e9 if x_ms > 0 else None
 
+    # ---- the same step through the fused exchange entry points (pad + tile +
+    # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
+    fused = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush)
     # ---- end to end: pinned host inputs copied in and the output copied out
     # every step, inside the timed region.  Copies run on their own stream so
     # step i+1's uploads and step i's download overlap step i's compute (two
@@ -305,6 +308,7 @@ def run_ours(args, world, rank, local):
                           "launches_per_step": step.n_exchange_launches(),
                           "bytes_per_launch": step.exchange_bytes_per_launch()},
         "stage_ms": {k: round(v / stage_n[k], 4) for k, v in stage_ms.items()},
+        "fused_step": fused,
         "e2e": {"value": round(weak_scaling_value(flops, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "copies": "pinned host buffers; H2D of step i+1 and D2H of step i overlap step i's compute"},
@@ -323,6 +327,43 @@ def run_ours(args, world, rank, local):
                                   "sample": f"{nrows} random output rows of {wl.name}, each over all {wl.T} keys "
                                             f"(fp64 C oracle, {secs:.1f} s)"}
     return result
+
+
+def time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush) -> dict:
+    """Device-resident timing of the step built with ``fused=True`` (same
+    inputs, same output bits), reported beside the staged step."""
+    import sequence_video_dit_gb300 as sp
+    from sequence_video_dit_gb300.step import StageTimer
+
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, device=dev,
+                     fused=True)
+    for _ in range(args.warmup):
+        step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
+    timer = StageTimer()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n0 = sp.lib().sp_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if not big_inputs:
+            flush.zero_()
+        starts[i].record()
+        step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um, timer=timer)
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = int(sp.lib().sp_launch_count() - n0)
+    st = sp.sp_workspace_status(step.ws_exchange)[0] | sp.sp_workspace_status(step.ws_attn)[0]
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the fused step")
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
+    tot, cnt = timer.totals_ms(), timer.counts()
+    out = {"value": round(weak_scaling_value(flops, world, ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+           "stage_ms": {k: round(v / cnt[k], 4) for k, v in tot.items()}, "gpu_launches": launches}
+    del step
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev) -> float:

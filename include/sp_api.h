@@ -157,6 +157,26 @@ SP_API int sp_send_recv_heads(const void *const *shards, void *const *heads, int
 SP_API int sp_gather_heads(const void *const *heads, void *const *shards, int W, int B, int Tl, int H,
                     int D, int elt_bytes, void *workspace, sp_stream_t stream);
 
+/* The exchange fused with its neighbours on one GPU, where the token shards
+ * need not exist (the survey of the pages' follow-up work: pad and tile fused
+ * with the send; the inverse exchange fused with gather_output).
+ *
+ * sp_pad_send_heads = sp_pad + sp_tile + sp_send_recv_heads in one pass over
+ * the caller's x [B, T, H, D]:
+ *   heads[r][b, g, h', :] = x[b, g, r*Hl + h', :]  for g < T,  0 for T <= g < T_pad.
+ * heads[r]: [B, T_pad, Hl, D].  T <= T_pad; T_pad % W != 0 gives
+ * SP_ERR_NOT_DIVISIBLE, H % W != 0 SP_ERR_HEADS_NOT_DIVISIBLE.  Same SM
+ * rotation, completion counters and workspace rules as sp_send_recv_heads. */
+SP_API int sp_pad_send_heads(const void *x, void *const *heads, int W, int B, int T, int T_pad, int H, int D,
+                             int elt_bytes, void *workspace, sp_stream_t stream);
+
+/* sp_gather_heads_output = sp_gather_heads + sp_gather_output (cropped to
+ * T_out, which is the unpad when T_out = T) in one pass:
+ *   out[b, g, r*Hl + h', :] = heads[r][b, g, h', :]  for g < T_out <= T_pad.
+ * out: [B, T_out, H, D].  Same rotation, counters and workspace rules. */
+SP_API int sp_gather_heads_output(const void *const *heads, void *out, int W, int B, int T_pad, int T_out, int H,
+                                  int D, int elt_bytes, void *workspace, sp_stream_t stream);
+
 /* sp_send_recv_heads without a caller workspace, for callers that cannot
  * allocate device memory: for example a plugin that is handed tensors by a
  * host framework whose allocator it cannot reach, or an inference loop that

@@ -28,7 +28,8 @@ from ._lib import (SP_BF16, SP_F32, SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_
 
 __all__ = [
     "sp_padded_len", "sp_partition", "sp_pad", "sp_pad_mask", "sp_tile", "sp_send_recv_heads",
-    "sp_gather_heads", "sp_send_recv_heads_noalloc", "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
+    "sp_gather_heads", "sp_send_recv_heads_noalloc", "sp_pad_send_heads", "sp_gather_heads_output",
+    "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
     "sp_workspace_status", "sp_sm_rotation_counts", "sp_exchange_grid", "new_workspace", "SPError",
     "SPValueError", "SPStep", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
 ]
@@ -52,6 +53,20 @@ def _need_cuda(*ts):
             raise SPValueError(3, "expected CUDA tensors")
         if not t.is_contiguous():
             raise SPValueError(3, "expected contiguous tensors")
+
+
+def _same(ts, shape, dtype, what):
+    """Every tensor of a per-rank list has the given shape and dtype (the
+    kernels index each buffer by these sizes)."""
+    for i, t in enumerate(ts):
+        if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            raise SPValueError(3, f"{what}[{i}]: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+
+
+def _split_heads(H, W, what):
+    if W < 1 or H % W:
+        raise SPValueError(2, f"{what}: H={H} is not divisible by W={W}")
+    return H // W
 
 
 def new_workspace(nbytes: int = SP_WORKSPACE_HEADER_BYTES, device=None) -> torch.Tensor:
@@ -109,6 +124,9 @@ def sp_tile(x_pad: torch.Tensor, shards, stream=None):
     """x_pad [B,T_pad,...] -> shards[r] [B,T_pad/W,...]."""
     _need_cuda(x_pad, *shards)
     W = len(shards)
+    if W < 1 or x_pad.shape[1] % W:
+        raise SPValueError(1, f"total_tokens={x_pad.shape[1]} is not divisible by world_size={W}")
+    _same(shards, (x_pad.shape[0], x_pad.shape[1] // W, *x_pad.shape[2:]), x_pad.dtype, "shards")
     check(lib().sp_tile(x_pad.data_ptr(), ptr_array(shards), W, x_pad.shape[0], x_pad.shape[1],
                         _row_bytes(x_pad), stream_handle(stream)))
     return shards
@@ -120,6 +138,9 @@ def sp_send_recv_heads(shards, heads, workspace: torch.Tensor, stream=None):
     _need_cuda(*shards, *heads, workspace)
     W = len(shards)
     B, Tl, H, D = shards[0].shape
+    Hl = _split_heads(H, W, "sp_send_recv_heads")
+    _same(shards, (B, Tl, H, D), shards[0].dtype, "shards")
+    _same(heads, (B, W * Tl, Hl, D), shards[0].dtype, "heads")
     check(lib().sp_send_recv_heads(ptr_array(shards), ptr_array(heads), W, B, Tl, H, D,
                                    shards[0].element_size(), workspace.data_ptr(), stream_handle(stream)))
     return heads
@@ -133,6 +154,9 @@ def sp_send_recv_heads_noalloc(shards, heads, stream=None, read_status: bool = T
     _need_cuda(*shards, *heads)
     W = len(shards)
     B, Tl, H, D = shards[0].shape
+    Hl = _split_heads(H, W, "sp_send_recv_heads_noalloc")
+    _same(shards, (B, Tl, H, D), shards[0].dtype, "shards")
+    _same(heads, (B, W * Tl, Hl, D), shards[0].dtype, "heads")
     st = ctypes.c_int(-1)
     check(lib().sp_send_recv_heads_noalloc(ptr_array(shards), ptr_array(heads), W, B, Tl, H, D,
                                            shards[0].element_size(), ctypes.byref(st) if read_status else None,
@@ -140,11 +164,43 @@ def sp_send_recv_heads_noalloc(shards, heads, stream=None, read_status: bool = T
     return st.value if read_status else None
 
 
+def sp_pad_send_heads(x, heads, workspace: torch.Tensor, stream=None):
+    """Fused pad + tile + exchange: x [B,T,H,D] -> heads[r] [B,T_pad,H/W,D]."""
+    _need_cuda(x, *heads, workspace)
+    W = len(heads)
+    B, T, H, D = x.shape
+    T_pad = heads[0].shape[1]
+    Hl = _split_heads(H, W, "sp_pad_send_heads")
+    if T_pad < T:
+        raise SPValueError(3, f"sp_pad_send_heads: T_pad={T_pad} < T={T}")
+    _same(heads, (B, T_pad, Hl, D), x.dtype, "heads")
+    check(lib().sp_pad_send_heads(x.data_ptr(), ptr_array(heads), W, B, T, T_pad, H, D, x.element_size(),
+                                  workspace.data_ptr(), stream_handle(stream)))
+    return heads
+
+
+def sp_gather_heads_output(heads, out, workspace: torch.Tensor, stream=None):
+    """Fused inverse exchange + gather_output: heads[r] [B,T_pad,Hl,D] -> out [B,T_out,W*Hl,D]."""
+    _need_cuda(out, *heads, workspace)
+    W = len(heads)
+    B, T_pad, Hl, D = heads[0].shape
+    _same(heads, (B, T_pad, Hl, D), heads[0].dtype, "heads")
+    if tuple(out.shape) != (B, out.shape[1], W * Hl, D) or out.dtype != heads[0].dtype or out.shape[1] > T_pad:
+        raise SPValueError(3, f"sp_gather_heads_output: out must be [B, T_out <= {T_pad}, {W * Hl}, {D}]")
+    check(lib().sp_gather_heads_output(ptr_array(heads), out.data_ptr(), W, B, T_pad, out.shape[1], Hl * W, D,
+                                       out.element_size(), workspace.data_ptr(), stream_handle(stream)))
+    return out
+
+
 def sp_gather_heads(heads, shards, workspace: torch.Tensor, stream=None):
     """heads[r] [B,W*Tl,Hl,D] -> shards[s] [B,Tl,W*Hl,D] (inverse exchange)."""
     _need_cuda(*shards, *heads, workspace)
     W = len(heads)
     B, T_all, Hl, D = heads[0].shape
+    if T_all % W:
+        raise SPValueError(1, f"total_tokens={T_all} is not divisible by world_size={W}")
+    _same(heads, (B, T_all, Hl, D), heads[0].dtype, "heads")
+    _same(shards, (B, T_all // W, W * Hl, D), heads[0].dtype, "shards")
     check(lib().sp_gather_heads(ptr_array(heads), ptr_array(shards), W, B, T_all // W, Hl * W, D,
                                 heads[0].element_size(), workspace.data_ptr(), stream_handle(stream)))
     return shards
@@ -203,8 +259,8 @@ def sp_attention(q, k, v, o, workspace: torch.Tensor, mask_kind: int = SP_MASK_N
         raise SPValueError(3, "sp_attention: k and v must share strides")
     mptr = None
     if mask_kind != SP_MASK_NONE:
-        if mask is None or not mask.is_cuda or not mask.is_contiguous():
-            raise SPValueError(3, "sp_attention: mask must be a contiguous CUDA tensor")
+        if mask is None or not mask.is_cuda or not mask.is_contiguous() or mask.element_size() != 1:
+            raise SPValueError(3, "sp_attention: mask must be a contiguous uint8/bool CUDA tensor")
         want = Tk if mask_kind == SP_MASK_KEY else B * Tq * Tk
         if mask.numel() != want:
             raise SPValueError(3, f"sp_attention: mask has {mask.numel()} elements, expected {want}")
@@ -223,6 +279,9 @@ def sp_gather_output(shards, out: torch.Tensor, stream=None) -> torch.Tensor:
     _need_cuda(out, *shards)
     W = len(shards)
     B, Tl = shards[0].shape[:2]
+    _same(shards, shards[0].shape, out.dtype, "shards")
+    if out.shape[0] != B or out.shape[2:] != shards[0].shape[2:] or out.shape[1] > W * Tl:
+        raise SPValueError(3, f"sp_gather_output: out must be [B, T_out <= {W * Tl}, ...] like the shards")
     check(lib().sp_gather_output(ptr_array(shards), out.data_ptr(), W, B, Tl, out.shape[1], _row_bytes(out),
                                  stream_handle(stream)))
     return out
@@ -230,6 +289,9 @@ def sp_gather_output(shards, out: torch.Tensor, stream=None) -> torch.Tensor:
 
 def sp_unpad(x_pad: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
     _need_cuda(x_pad, out)
+    if (out.shape[0] != x_pad.shape[0] or out.shape[2:] != x_pad.shape[2:] or out.shape[1] > x_pad.shape[1]
+            or out.dtype != x_pad.dtype):
+        raise SPValueError(3, "sp_unpad: out must be [B, T <= T_pad, ...] like x_pad")
     check(lib().sp_unpad(x_pad.data_ptr(), out.data_ptr(), x_pad.shape[0], x_pad.shape[1], out.shape[1],
                          _row_bytes(x_pad), stream_handle(stream)))
     return out

@@ -49,6 +49,8 @@ SIGNATURES = {
     "sp_send_recv_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_gather_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_send_recv_heads_noalloc": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _IP, _P]),
+    "sp_pad_send_heads": (_I, [_P, _PP, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "sp_gather_heads_output": (_I, [_PP, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_workspace_status": (_I, [_P, _IP, _IP, _IP, _I, _P]),
     "sp_sm_rotation_counts": (_I, [_I, _I, _IP]),
     "sp_exchange_grid": (_I, [_IP]),

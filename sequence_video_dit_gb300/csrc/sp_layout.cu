@@ -195,6 +195,32 @@ struct ExchangeParams {
     WorkspaceHeader *ws;
 };
 
+// Completion barrier ("barrier" paragraph): make this CTA's writes visible,
+// then count it on its destination rank.  The last CTA to take a ticket checks
+// every counter against the CTA map, records the counts and resets them.
+__device__ __forceinline__ void exchange_complete(WorkspaceHeader *ws, int r, int W) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0 && ws != nullptr) {
+        atomicAdd(&ws->counters[r], 1);
+        __threadfence();
+        const int ticket = atomicAdd(&ws->ticket, 1);
+        if (ticket == (int)gridDim.x - 1) {
+            __threadfence();
+            for (int q = 0; q < SP_MAX_RANKS; q++) {
+                const int seen = atomicExch(&ws->counters[q], 0);
+                const int expect = q < W ? (int)((gridDim.x - q + W - 1) / W) : 0;
+                ws->observed[q] = seen;
+                if (seen != expect) set_device_status(&ws->status, SP_ERR_BARRIER);
+            }
+            ws->grid = (int)gridDim.x;
+            atomicAdd(&ws->launches, 1);
+            __threadfence();
+            atomicExch(&ws->ticket, 0);
+        }
+    }
+}
+
 // GATHER = false: send_recv_heads.  CTA i serves rank r = i % W (SM rotation)
 // and its rank group walks r's chunks c = (b, s*Tl + t) with a stride; the
 // destination heads[r] + c*chunk is contiguous, the source is the r-th head
@@ -222,32 +248,105 @@ __global__ void __launch_bounds__(256) exchange_kernel(ExchangeParams p, int nve
             copy_row<V>(p.dst[s] + tok_off, heads_src_r + (int64_t)c * p.chunk_bytes, nvec, lane, tx);
         }
     }
-    // Completion barrier: make this CTA's writes visible, then count it on its
-    // destination rank.  The last CTA to take a ticket checks all counters.
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0 && p.ws != nullptr) {
-        WorkspaceHeader *ws = p.ws;
-        atomicAdd(&ws->counters[r], 1);
-        __threadfence();
-        const int ticket = atomicAdd(&ws->ticket, 1);
-        if (ticket == (int)gridDim.x - 1) {
-            __threadfence();
-            for (int q = 0; q < SP_MAX_RANKS; q++) {
-                const int seen = atomicExch(&ws->counters[q], 0);
-                const int expect = q < W ? (int)((gridDim.x - q + W - 1) / W) : 0;
-                ws->observed[q] = seen;
-                if (seen != expect) set_device_status(&ws->status, SP_ERR_BARRIER);
-            }
-            ws->grid = (int)gridDim.x;
-            atomicAdd(&ws->launches, 1);
-            __threadfence();
-            atomicExch(&ws->ticket, 0);
+    exchange_complete(p.ws, r, W);
+}
+
+// The exchange fused with its neighbours, for a caller-held [B, T, H, D]
+// tensor x (one GPU: the token shards never need to exist).
+//   GATHER = false  (pad + tile + send_recv_heads):
+//     heads[r][b, g, h', :] = g < T ? x[b, g, r*Hl + h', :] : 0,   g < T_pad
+//   GATHER = true   (gather_heads + gather_output cropped to T_out):
+//     y[b, g, r*Hl + h', :] = heads[r][b, g, h', :],               g < T_out
+// Same SM rotation, chunk walk and completion barrier as exchange_kernel.
+struct FusedParams {
+    uint8_t *heads[SP_MAX_RANKS];
+    uint8_t *x;         // caller tensor: source (send) or destination (gather)
+    int W, T_real;      // T_real = T (send) or T_out (gather)
+    uint32_t T_pad;
+    uint32_t chunks_per_rank;  // B * T_pad
+    int64_t chunk_bytes, row_bytes;
+    WorkspaceHeader *ws;
+};
+
+template <int V, bool GATHER>
+__global__ void __launch_bounds__(256) exchange_fused_kernel(FusedParams p, int nvec, int tx_log2) {
+    const int W = p.W;
+    const int r = blockIdx.x % W;
+    const uint32_t grp = blockIdx.x / W;
+    const uint32_t n_r = (gridDim.x - r + W - 1) / W;
+    const int tx = 1 << tx_log2;
+    const int lane = threadIdx.x & (tx - 1);
+    const uint32_t groups_per_cta = blockDim.x >> tx_log2;
+    const uint32_t gid = grp * groups_per_cta + (threadIdx.x >> tx_log2);
+    const uint32_t ngroups = n_r * groups_per_cta;
+    uint8_t *const heads_r = p.heads[r];
+    for (uint32_t c = gid; c < p.chunks_per_rank; c += ngroups) {
+        const uint32_t b = c / p.T_pad, g = c - b * p.T_pad;
+        const bool real = g < (uint32_t)p.T_real;
+        const int64_t x_off = ((int64_t)b * p.T_real + g) * p.row_bytes + (int64_t)r * p.chunk_bytes;
+        if (!GATHER) {
+            copy_row<V>(heads_r + (int64_t)c * p.chunk_bytes, real ? p.x + x_off : nullptr, nvec, lane, tx);
+        } else if (real) {
+            copy_row<V>(p.x + x_off, heads_r + (int64_t)c * p.chunk_bytes, nvec, lane, tx);
         }
     }
+    exchange_complete(p.ws, r, W);
 }
 
 static int exchange_grid(const DeviceInfo &di) { return di.num_sms * 4; }
+
+template <bool GATHER>
+static int launch_exchange_fused(void *x, void *const *heads, int W, int B, int T_pad, int T_real, int H, int D,
+                                 int elt, void *workspace, cudaStream_t st, const char *what) {
+    if (W < 1 || W > SP_MAX_RANKS) return set_error(SP_ERR_INVALID_ARG, "%s: W=%d out of [1,%d]", what, W, SP_MAX_RANKS);
+    if (B < 0 || T_pad < 0 || T_real < 0 || T_real > T_pad || H < 1 || D < 1)
+        return set_error(SP_ERR_INVALID_ARG, "%s: bad sizes", what);
+    if (elt != 1 && elt != 2 && elt != 4 && elt != 8) return set_error(SP_ERR_INVALID_ARG, "%s: elt_bytes=%d", what, elt);
+    if (T_pad % W != 0)
+        return set_error(SP_ERR_NOT_DIVISIBLE, "total_tokens=%d is not divisible by world_size=%d", T_pad, W);
+    if (H % W != 0) return set_error(SP_ERR_HEADS_NOT_DIVISIBLE, "%s: H=%d is not divisible by W=%d", what, H, W);
+    if (!heads || !workspace) return set_error(SP_ERR_INVALID_ARG, "%s: null pointer array or workspace", what);
+    if (((uintptr_t)workspace & 15) != 0) return set_error(SP_ERR_ALIGNMENT, "%s: workspace not 16-byte aligned", what);
+    const int Hl = H / W;
+    FusedParams p;
+    memset(&p, 0, sizeof(p));
+    p.chunk_bytes = (int64_t)Hl * D * elt;
+    p.row_bytes = (int64_t)H * D * elt;
+    uint64_t align = (uint64_t)p.chunk_bytes;
+    const bool any = (int64_t)B * T_pad > 0;
+    if (any && T_real > 0 && !x) return set_error(SP_ERR_INVALID_ARG, "%s: null tensor", what);
+    p.x = (uint8_t *)x;
+    align |= (uint64_t)(uintptr_t)x;
+    for (int i = 0; i < W; i++) {
+        if (any && !heads[i]) return set_error(SP_ERR_INVALID_ARG, "%s: null buffer for rank %d", what, i);
+        p.heads[i] = (uint8_t *)heads[i];
+        align |= (uint64_t)(uintptr_t)heads[i];
+    }
+    const int V = vector_width(align ? align : 16);
+    p.W = W;
+    p.T_real = T_real;
+    p.T_pad = (uint32_t)T_pad;
+    const uint64_t chunks = (uint64_t)B * T_pad;
+    if (chunks > 0x7fffffffull) return set_error(SP_ERR_INVALID_ARG, "%s: too many tokens", what);
+    p.chunks_per_rank = (uint32_t)chunks;
+    p.ws = (WorkspaceHeader *)workspace;
+    if (chunks == 0) return SP_OK;
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    const int nvec = (int)(p.chunk_bytes / V);
+    const int tl = tx_log2_for(nvec);
+    int grid = exchange_grid(di);
+    if (grid < W) grid = W;
+    switch (V) {
+        case 16: exchange_fused_kernel<16, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
+        case 8: exchange_fused_kernel<8, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
+        case 4: exchange_fused_kernel<4, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
+        case 2: exchange_fused_kernel<2, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
+        default: exchange_fused_kernel<1, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
+    }
+    return check_launch(what);
+}
 
 template <bool GATHER>
 static int launch_exchange(const void *const *src, void *const *dst, int W, int B, int Tl, int H,
@@ -490,6 +589,18 @@ int sp_send_recv_heads_noalloc(const void *const *shards, void *const *heads, in
         SP_CUDA_CHECK(cudaMemsetAsync(ws, 0, sizeof(int), st));
     }
     return SP_OK;
+}
+
+int sp_pad_send_heads(const void *x, void *const *heads, int W, int B, int T, int T_pad, int H, int D,
+                      int elt_bytes, void *workspace, sp_stream_t stream) {
+    return launch_exchange_fused<false>(const_cast<void *>(x), heads, W, B, T_pad, T, H, D, elt_bytes, workspace,
+                                        (cudaStream_t)stream, "sp_pad_send_heads");
+}
+
+int sp_gather_heads_output(const void *const *heads, void *out, int W, int B, int T_pad, int T_out, int H, int D,
+                           int elt_bytes, void *workspace, sp_stream_t stream) {
+    return launch_exchange_fused<true>(out, const_cast<void *const *>(heads), W, B, T_pad, T_out, H, D, elt_bytes,
+                                       workspace, (cudaStream_t)stream, "sp_gather_heads_output");
 }
 
 int sp_workspace_status(void *workspace, int *status, int *counts, int *n_launches, int clear,

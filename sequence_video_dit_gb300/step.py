@@ -17,14 +17,18 @@ breakdown), sections 补齐 -> 切分 -> 换头 -> 还原:
 Each virtual rank owns separate device allocations.  sp_pad is skipped when T
 is already a multiple of W (padding is then the identity).  Host code here
 only allocates buffers and issues library calls on the current stream.
+
+``fused=True`` runs the same step with the fused exchange entry points: one
+sp_pad_send_heads per tensor (pad + tile + exchange in one pass, no token-shard
+buffers) and one sp_gather_heads_output (inverse exchange + gather + unpad).
 """
 from __future__ import annotations
 
 import torch
 
 from . import (SP_MASK_FULL, SP_MASK_KEY, new_workspace, sp_attention, sp_attention_workspace_bytes,
-               sp_gather_heads, sp_gather_output, sp_pad, sp_pad_mask, sp_padded_len, sp_partition,
-               sp_send_recv_heads, sp_tile, SPValueError)
+               sp_gather_heads, sp_gather_heads_output, sp_gather_output, sp_pad, sp_pad_mask, sp_pad_send_heads,
+               sp_padded_len, sp_partition, sp_send_recv_heads, sp_tile, SPValueError)
 
 
 class _NullTimer:
@@ -78,7 +82,7 @@ class SPStep:
     """
 
     def __init__(self, W: int, B: int, T: int, H: int, D: int, dtype=torch.bfloat16, mask: str = "key",
-                 Tq: int | None = None, device=None):
+                 Tq: int | None = None, device=None, fused: bool = False):
         if H % W:
             raise SPValueError(2, f"H={H} is not divisible by W={W}")
         if mask not in ("key", "user"):
@@ -95,15 +99,16 @@ class SPStep:
         self.Tl = self.T_pad // W
         self.Hl = H // W
         self.need_pad = self.T_pad != T
+        self.fused = fused
         names = ("k", "v") if self.cross else ("q", "k", "v")
         self.names = names
         emp = lambda *shape: torch.empty(*shape, dtype=dtype, device=dev)  # noqa: E731
-        self.xpad = {n: emp(B, self.T_pad, H, D) for n in names} if self.need_pad else {}
-        self.shards = {n: [emp(B, self.Tl, H, D) for _ in range(W)] for n in names}
+        self.xpad = {n: emp(B, self.T_pad, H, D) for n in names} if (self.need_pad and not fused) else {}
+        self.shards = {} if fused else {n: [emp(B, self.Tl, H, D) for _ in range(W)] for n in names}
         self.heads = {n: [emp(B, self.T_pad, self.Hl, D) for _ in range(W)] for n in names}
         if not self.cross:
             self.o_heads = [emp(B, self.T_pad, self.Hl, D) for _ in range(W)]
-            self.o_shards = [emp(B, self.Tl, H, D) for _ in range(W)]
+            self.o_shards = [] if fused else [emp(B, self.Tl, H, D) for _ in range(W)]
             self.out = emp(B, T, H, D)
             Tq_att = self.T_pad
         else:
@@ -121,6 +126,7 @@ class SPStep:
         return 2 * self.B * self.T_pad * self.H * self.D * torch.empty((), dtype=self.dtype).element_size()
 
     def n_exchange_launches(self) -> int:
+        """Launches of the exchange kernels per step (send per tensor + gather)."""
         return len(self.names) + (0 if self.cross else 1)
 
     def __call__(self, q, k, v, user_mask=None, timer=None, out=None):
@@ -133,7 +139,7 @@ class SPStep:
             raise SPValueError(3, "out must match the step's output shape and dtype")
         src = {"q": q, "k": k, "v": v}
         with t("pad"):
-            if self.need_pad:
+            if self.need_pad and not self.fused:
                 for n in self.names:
                     sp_pad(src[n], self.xpad[n])
             if self.mask_kind == "key":
@@ -142,12 +148,17 @@ class SPStep:
                 if user_mask is None:
                     raise SPValueError(3, "this step was built for a user mask")
                 sp_pad_mask(user_mask, self.mask, self.T)
-        with t("tile"):
-            for n in self.names:
-                sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
-        with t("send_recv_heads"):
-            for n in self.names:
-                sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
+        if self.fused:
+            with t("send_recv_heads"):
+                for n in self.names:
+                    sp_pad_send_heads(src[n], self.heads[n], self.ws_exchange)
+        else:
+            with t("tile"):
+                for n in self.names:
+                    sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
+            with t("send_recv_heads"):
+                for n in self.names:
+                    sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
         kind = SP_MASK_KEY if self.mask_kind == "key" else SP_MASK_FULL
         mask = self.mask.view(-1) if kind == SP_MASK_KEY else self.mask
         Hl, D = self.Hl, self.D
@@ -160,8 +171,12 @@ class SPStep:
                 ov = [out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(self.W)]
                 sp_attention(qv, self.heads["k"], self.heads["v"], ov, self.ws_attn, kind, mask)
         if not self.cross:
-            with t("gather_heads"):
-                sp_gather_heads(self.o_heads, self.o_shards, self.ws_exchange)
-            with t("gather_output"):
-                sp_gather_output(self.o_shards, out)
+            if self.fused:
+                with t("gather_heads"):
+                    sp_gather_heads_output(self.o_heads, out, self.ws_exchange)
+            else:
+                with t("gather_heads"):
+                    sp_gather_heads(self.o_heads, self.o_shards, self.ws_exchange)
+                with t("gather_output"):
+                    sp_gather_output(self.o_shards, out)
         return out

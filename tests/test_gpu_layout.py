@@ -165,3 +165,60 @@ def test_full_size_exchange_round_trip_and_sampled_map():
         assert np.array_equal(bytes_np(heads[r][:, rows]), mini_heads[r])
     torch.cuda.synchronize()
     assert sp.sp_workspace_status(ws)[0] == 0
+
+
+@pytest.mark.parametrize("B,T,W,H,D,dtype", CASES)
+def test_fused_exchange_bit_exact(B, T, W, H, D, dtype):
+    # sp_pad_send_heads == pad -> tile -> send_recv_heads, and
+    # sp_gather_heads_output == gather_heads -> gather_output (cropped to T).
+    g = torch.Generator().manual_seed(7 * T + W)
+    x = random_bytes((B, T, H, D), dtype, g)
+    T_pad = sp.sp_padded_len(T, W)
+    Hl = H // W
+    ws = sp.new_workspace()
+    heads = [torch.full((B, T_pad, Hl, D), 1.0, dtype=dtype, device="cuda") for _ in range(W)]
+    sp.sp_pad_send_heads(x, heads, ws)
+    want = oracle.send_recv_heads(oracle.tile(oracle.pad(bytes_np(x), T_pad), W))
+    for r in range(W):
+        assert np.array_equal(bytes_np(heads[r]), want[r])
+    out = torch.empty(B, T, H, D, dtype=dtype, device="cuda")
+    sp.sp_gather_heads_output(heads, out, ws)
+    want_out = oracle.gather_output(oracle.gather_heads([bytes_np(h) for h in heads]), T)
+    assert np.array_equal(bytes_np(out), want_out)
+    assert torch.equal(out.view(torch.uint8), x.view(torch.uint8))  # round trip
+    torch.cuda.synchronize()
+    st, counts, n = sp.sp_workspace_status(ws)
+    assert st == 0 and n == 2
+    assert counts[:W] == oracle.sm_rotation_counts(sp.sp_exchange_grid(), W)
+
+
+def test_fused_exchange_argument_errors():
+    x = torch.zeros(1, 10, 6, 8, dtype=torch.bfloat16, device="cuda")
+    heads = [torch.zeros(1, 12, 1, 8, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    with pytest.raises(ValueError):  # H = 6 not divisible by W = 4
+        sp.sp_pad_send_heads(x, heads, sp.new_workspace())
+    x = torch.zeros(1, 10, 4, 8, dtype=torch.bfloat16, device="cuda")
+    heads = [torch.zeros(1, 11, 1, 8, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    with pytest.raises(ValueError):  # T_pad = 11 is not a multiple of W = 4
+        sp.sp_pad_send_heads(x, heads, sp.new_workspace())
+
+
+def test_mismatched_rank_buffers_are_rejected_before_launch():
+    W, B, Tl, H, D = 4, 1, 8, 8, 16
+    shards = [torch.zeros(B, Tl, H, D, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    heads = [torch.zeros(B, W * Tl, H // W, D, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    short = heads[:3] + [torch.zeros(B, W * Tl - 1, H // W, D, dtype=torch.bfloat16, device="cuda")]
+    with pytest.raises(ValueError):
+        sp.sp_send_recv_heads(shards, short, sp.new_workspace())
+    with pytest.raises(ValueError):
+        sp.sp_gather_heads(short, shards, sp.new_workspace())
+    with pytest.raises(ValueError):
+        sp.sp_pad_send_heads(torch.zeros(B, 30, H, D, dtype=torch.bfloat16, device="cuda"), short,
+                             sp.new_workspace())
+    with pytest.raises(ValueError):  # out longer than the padded length
+        sp.sp_gather_heads_output(heads, torch.zeros(B, W * Tl + 1, H, D, dtype=torch.bfloat16, device="cuda"),
+                                  sp.new_workspace())
+    with pytest.raises(ValueError):
+        sp.sp_tile(torch.zeros(B, W * Tl, H, D, device="cuda"), [torch.zeros(B, Tl + 1, H, D, device="cuda")] * W)
+    with pytest.raises(ValueError):
+        sp.sp_unpad(torch.zeros(B, 8, H, D, device="cuda"), torch.zeros(B, 9, H, D, device="cuda"))

@@ -114,3 +114,18 @@ def test_step_is_repeatable():
     a = step(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
     b = step(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_fused_step_equals_staged_step_bitwise(name):
+    # The fused exchange entry points move the same bytes to the same places,
+    # so the whole step gives the same output bit for bit.
+    wl = workloads.get(name)
+    inp, dev, um = _inputs(wl)
+    staged = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq)
+    fused = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, fused=True)
+    a = staged(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    b = fused(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(fused.ws_exchange)[0] == 0
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
