@@ -3,7 +3,7 @@
 The call sequence follows "LTX-2 序列并行拆解" (LTX-2 sequence-parallel
 breakdown), sections 补齐 -> 切分 -> 换头 -> 还原:
 
-  self-attention                        cross-attention (small query modality)
+  self-attention                        cross-attention, small query modality
   1 sp_pad(Q,K,V), sp_pad_mask          1 sp_pad(K,V), sp_pad_mask (key mask)
   2 sp_tile(Q,K,V)                      2 sp_tile(K,V)
   3 sp_send_recv_heads(Q,K,V)           3 sp_send_recv_heads(K,V)  (Q is sliced
@@ -13,6 +13,14 @@ breakdown), sections 补齐 -> 切分 -> 换头 -> 还原:
   5 sp_gather_heads(O)
   6 sp_gather_output(O) cropped to the caller's length T (each rank's real
     token count), which is the unpad
+
+The small-query case is the pages' video->audio direction: the audio query
+stays whole on every rank and only the video K/V go through the exchange.
+The opposite direction (``Tkv``: video queries attend a small, replicated
+audio K/V) mirrors it: Q is padded, tiled and exchanged like self-attention,
+each rank reads its heads of K/V in place, and O returns through
+gather_heads / gather_output.  Pad query rows then see every audio key; they
+are cropped by the unpad.
 
 Each virtual rank owns separate device allocations.  sp_pad is skipped when T
 is already a multiple of W (padding is then the identity).  Host code here
@@ -74,25 +82,34 @@ class StageTimer:
 class SPStep:
     """Buffers and call sequence of one SP attention step.
 
-    Self-attention: ``Tq=None``, inputs q/k/v [B,T,H,D].
-    Cross-attention: ``Tq`` query tokens (replicated on every rank), q
-    [B,Tq,H,D]; k/v [B,T,H,D] go through the exchange.
+    ``T`` is always the length of the token-sharded sequence.
+    Self-attention: ``Tq=Tkv=None``, inputs q/k/v [B,T,H,D].
+    Cross-attention, small query: ``Tq`` query tokens (replicated on every
+    rank), q [B,Tq,H,D]; k/v [B,T,H,D] go through the exchange.
+    Cross-attention, small K/V: ``Tkv`` key tokens (replicated on every rank),
+    q [B,T,H,D] goes through the exchange; k/v [B,Tkv,H,D], every key valid.
     ``mask``: "key" (key-only padding mask) or "user" ((B,T,T) user mask,
     self-attention only).
     """
 
     def __init__(self, W: int, B: int, T: int, H: int, D: int, dtype=torch.bfloat16, mask: str = "key",
-                 Tq: int | None = None, device=None, fused: bool = False):
+                 Tq: int | None = None, device=None, fused: bool = False, Tkv: int | None = None):
         if H % W:
             raise SPValueError(2, f"H={H} is not divisible by W={W}")
         if mask not in ("key", "user"):
             raise SPValueError(3, f"mask must be 'key' or 'user', got {mask!r}")
-        if Tq is not None and mask == "user":
+        if (Tq is not None or Tkv is not None) and mask == "user":
             raise SPValueError(3, "cross-attention takes the key-only mask")
+        if Tq is not None and Tkv is not None:
+            raise SPValueError(3, "give Tq (small query) or Tkv (small K/V), not both")
+        if Tkv is not None and Tkv < 0:
+            raise SPValueError(3, f"Tkv={Tkv} < 0")
         dev = torch.device(device or "cuda")
         self.W, self.B, self.T, self.H, self.D, self.dtype = W, B, T, H, D, dtype
         self.cross = Tq is not None
         self.Tq = Tq if self.cross else None
+        self.kv_small = Tkv is not None
+        self.Tkv = Tkv
         self.mask_kind = mask
         self.T_pad = sp_padded_len(T, W)
         sp_partition(self.T_pad, W)
@@ -100,7 +117,7 @@ class SPStep:
         self.Hl = H // W
         self.need_pad = self.T_pad != T
         self.fused = fused
-        names = ("k", "v") if self.cross else ("q", "k", "v")
+        names = ("k", "v") if self.cross else (("q",) if self.kv_small else ("q", "k", "v"))
         self.names = names
         emp = lambda *shape: torch.empty(*shape, dtype=dtype, device=dev)  # noqa: E731
         self.xpad = {n: emp(B, self.T_pad, H, D) for n in names} if (self.need_pad and not fused) else {}
@@ -114,12 +131,15 @@ class SPStep:
         else:
             self.out = emp(B, Tq, H, D)
             Tq_att = Tq
-        if mask == "key":
+        if self.kv_small:
+            self.mask = None  # every replicated key is valid
+        elif mask == "key":
             self.mask = torch.empty(1, 1, self.T_pad, dtype=torch.uint8, device=dev)
         else:
             self.mask = torch.empty(B, self.T_pad, self.T_pad, dtype=torch.uint8, device=dev)
+        Tk_att = Tkv if self.kv_small else self.T_pad
         self.ws_exchange = new_workspace(device=dev)
-        self.ws_attn = new_workspace(sp_attention_workspace_bytes(W, B, Tq_att, self.T_pad, self.Hl, D, dtype), dev)
+        self.ws_attn = new_workspace(sp_attention_workspace_bytes(W, B, Tq_att, Tk_att, self.Hl, D, dtype), dev)
 
     # bytes each exchange launch reads + writes
     def exchange_bytes_per_launch(self) -> int:
@@ -142,7 +162,9 @@ class SPStep:
             if self.need_pad and not self.fused:
                 for n in self.names:
                     sp_pad(src[n], self.xpad[n])
-            if self.mask_kind == "key":
+            if self.mask is None:
+                pass  # small replicated K/V: no padding mask
+            elif self.mask_kind == "key":
                 sp_pad_mask(None, self.mask, self.T)
             else:
                 if user_mask is None:
@@ -160,10 +182,13 @@ class SPStep:
                 for n in self.names:
                     sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
         kind = SP_MASK_KEY if self.mask_kind == "key" else SP_MASK_FULL
-        mask = self.mask.view(-1) if kind == SP_MASK_KEY else self.mask
+        mask = None if self.mask is None else (self.mask.view(-1) if kind == SP_MASK_KEY else self.mask)
         Hl, D = self.Hl, self.D
         with t("attention"):
-            if not self.cross:
+            if self.kv_small:
+                kv = [(k[:, :, r * Hl:(r + 1) * Hl, :], v[:, :, r * Hl:(r + 1) * Hl, :]) for r in range(self.W)]
+                sp_attention(self.heads["q"], [a for a, _ in kv], [b for _, b in kv], self.o_heads, self.ws_attn)
+            elif not self.cross:
                 sp_attention(self.heads["q"], self.heads["k"], self.heads["v"], self.o_heads, self.ws_attn,
                              kind, mask)
             else:

@@ -129,3 +129,32 @@ def test_fused_step_equals_staged_step_bitwise(name):
     torch.cuda.synchronize()
     assert sp.sp_workspace_status(fused.ws_exchange)[0] == 0
     assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("W,B,T,Tkv,H,D,dtype,fused", [
+    (2, 2, 37, 20, 4, 32, torch.float32, False),     # CUDA-core path, ragged pad
+    (8, 1, 6149, 1001, 32, 128, torch.bfloat16, False),  # video 6149 tokens x audio 1001
+    (8, 1, 6149, 1001, 32, 128, torch.bfloat16, True),
+    (4, 2, 1001, 250, 8, 64, torch.bfloat16, True),
+])
+def test_small_kv_cross_attention(W, B, T, Tkv, H, D, dtype, fused):
+    # Video queries (token-sharded, exchanged) attend a small audio K/V that
+    # every rank holds whole and slices by head in place.
+    wl = workloads.make_custom("a2v", W=W, B=B, T=Tkv, H=H, D=D, dtype="f32" if dtype == torch.float32 else "bf16",
+                               Tq=T, index=200 + T % 97)
+    inp = workloads.make_inputs(wl)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    step = sp.SPStep(W, B, T, H, D, dtype=dtype, Tkv=Tkv, fused=fused)
+    out = f32_np(step(dev["q"], dev["k"], dev["v"]))
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    assert sp.sp_workspace_status(step.ws_attn)[0] == 0
+    assert out.shape == (B, T, H, D) and np.isfinite(out).all()
+    q, k, v = (inp[n].float().numpy() for n in ("q", "k", "v"))
+    if T * Tkv * H * B <= 1_000_000:
+        ref = oracle.attention(q, k, v)
+        assert max_abs(out, ref) <= tol_for(dtype)
+    else:
+        rows = _sample_rows(B, T, H, 256, wl.seed)
+        ref = oracle.attention_rows(q, k, v, rows)
+        assert max_abs(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= tol_for(dtype)
