@@ -74,6 +74,12 @@ def _L():
             lib.oracle_gather_output.argtypes = [P, P, I, I, I, I, Z]
             lib.oracle_unpad.argtypes = [P, P, I, I, I, Z]
             lib.oracle_sm_rotation_counts.argtypes = [I, I, P]
+            lib.oracle_optimal_split.argtypes = [I, P, P]
+            lib.oracle_optimal_split.restype = I
+            lib.oracle_tile_2d.argtypes = [P, P, I, I, I, I, I, I, Z]
+            lib.oracle_tile_2d.restype = I
+            lib.oracle_gather_2d.argtypes = [P, P, I, I, I, I, I, I, Z]
+            lib.oracle_gather_2d.restype = I
             lib.oracle_attention.argtypes = [P, P, P, P, I, I, I, I, I, I, P, D_, I]
             lib.oracle_attention.restype = I
             lib.oracle_attention_rows.argtypes = [P, P, P, P, I, I, I, I, I, I, P, D_, P, I64, I]
@@ -205,6 +211,63 @@ def unpad(x_pad: np.ndarray, T: int) -> np.ndarray:
     return out
 
 
+# ---------------------------------------------------------------- 2-D spatial split
+# LongCat-Video context parallel ("智能张量拆分"): an alternative to the
+# token-range partition for the tile step.  The latent tokens of a batch item
+# are a [F, Hg, Wg] grid (frames x patch rows x patch columns) in row-major
+# order.
+class SplitError(ValueError):
+    """The grid is not divisible by the 2-D split."""
+
+
+def optimal_split(W: int):
+    """(split_h, split_w): the factor pair of W closest to a square, the
+    smaller factor on height.  Pinned: brute force over all factor pairs."""
+    sh = ctypes.c_int(0)
+    sw = ctypes.c_int(0)
+    if _L().oracle_optimal_split(W, ctypes.byref(sh), ctypes.byref(sw)) != 0:
+        raise ValueError(f"W={W} < 1")
+    return sh.value, sw.value
+
+
+def tile_2d(x: np.ndarray, grid, split):
+    """x [B, F*Hg*Wg, ...] -> split_h*split_w shards [B, F*(Hg/split_h)*(Wg/split_w), ...];
+    rank ih*split_w + iw holds block (ih, iw) of every frame.  Pinned:
+    hand-enumerated fixtures, reduction to ``tile`` for one-band splits, round
+    trip with gather_2d."""
+    F, Hg, Wg = grid
+    sh, sw = split
+    x = np.ascontiguousarray(x)
+    B, T = x.shape[:2]
+    if T != F * Hg * Wg:
+        raise ValueError("token count does not match the grid")
+    if Hg % sh or Wg % sw:
+        raise SplitError(f"grid {Hg}x{Wg} is not divisible by the split {sh}x{sw}")
+    Tl = F * (Hg // sh) * (Wg // sw)
+    shards = [np.empty((B, Tl) + x.shape[2:], dtype=x.dtype) for _ in range(sh * sw)]
+    rc = _L().oracle_tile_2d(_p(x), _ptr_array(shards), B, F, Hg, Wg, sh, sw, _row_bytes(x, 2))
+    if rc:
+        raise SplitError("tile_2d failed")
+    return shards
+
+
+def gather_2d(shards, grid, split) -> np.ndarray:
+    """Inverse of tile_2d: shards -> [B, F*Hg*Wg, ...]."""
+    F, Hg, Wg = grid
+    sh, sw = split
+    if len(shards) != sh * sw:
+        raise ValueError("one shard per rank of the split")
+    if Hg % sh or Wg % sw:
+        raise SplitError(f"grid {Hg}x{Wg} is not divisible by the split {sh}x{sw}")
+    shards = [np.ascontiguousarray(s) for s in shards]
+    B = shards[0].shape[0]
+    out = np.empty((B, F * Hg * Wg) + shards[0].shape[2:], dtype=shards[0].dtype)
+    rc = _L().oracle_gather_2d(_ptr_array(shards), _p(out), B, F, Hg, Wg, sh, sw, _row_bytes(shards[0], 2))
+    if rc:
+        raise SplitError("gather_2d failed")
+    return out
+
+
 def sm_rotation_counts(n_sm: int, W: int):
     """#SMs serving each rank when SM i writes rank i % W.  Pinned: the page's
     132-SM / 8-GPU example."""
@@ -303,3 +366,19 @@ def sp_step(q, k, v, W: int, user_mask=None, scale: float | None = None,
     o = unpad(o, T)
     stages.update(mask=mask, o_heads=o_heads, o_shards=o_shards)
     return (o, stages) if return_stages else o
+
+
+def sp_step_2d(q, k, v, grid, W: int, scale: float | None = None, threads: int | None = None):
+    """The sharded step with the 2-D spatial split in place of pad + tile:
+    tile_2d -> send_recv_heads -> per-rank attention -> gather_heads ->
+    gather_2d.  No padding (the split must divide the grid), no mask.
+    Self-attention on [B, F*Hg*Wg, H, D]; returns float64.  Pinned: equals
+    unsharded ``attention`` up to the order of the key sum."""
+    B, T, H, D = q.shape
+    if H % W:
+        raise ValueError("H is not divisible by world_size")
+    split = optimal_split(W)
+    heads = {n: send_recv_heads(tile_2d(x, grid, split)) for n, x in (("q", q), ("k", k), ("v", v))}
+    o_heads = [attention(heads["q"][r], heads["k"][r], heads["v"][r], MASK_NONE, None, scale, threads)
+               for r in range(W)]
+    return gather_2d(gather_heads(o_heads), grid, split)

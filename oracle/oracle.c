@@ -165,6 +165,72 @@ void oracle_unpad(const uint8_t *x_pad, uint8_t *out, int B, int T_pad, int T, s
 }
 
 /* ------------------------------------------------------------------ */
+/* 2-D spatial split (LongCat-Video context parallel, "智能张量拆分"): the
+ * world size is factored as split_h x split_w, the factor pair closest to a
+ * square (split_h <= split_w); every frame of the latent grid [F, Hg, Wg] is
+ * cut into split_h bands of height and each band into split_w pieces of
+ * width; rank r = ih * split_w + iw receives piece (ih, iw) of every frame,
+ * tokens in (frame, row, column) order.  Block sizes are Hg / split_h and
+ * Wg / split_w; a grid they do not divide is an error (return 1). */
+int oracle_optimal_split(int W, int *split_h, int *split_w) {
+    if (W < 1) return 2;
+    int best_a = 1, best_gap = W - 1;
+    for (int a = 1; a <= W; a++) {
+        if (W % a != 0) continue;
+        int b = W / a;
+        if (a > b) continue;
+        if (b - a < best_gap) {
+            best_gap = b - a;
+            best_a = a;
+        }
+    }
+    *split_h = best_a;
+    *split_w = W / best_a;
+    return 0;
+}
+
+int oracle_tile_2d(const uint8_t *x, uint8_t **shards, int B, int F, int Hg, int Wg, int split_h,
+                   int split_w, size_t row_bytes) {
+    if (split_h < 1 || split_w < 1 || Hg % split_h != 0 || Wg % split_w != 0) return 1;
+    int bh = Hg / split_h, bw = Wg / split_w;
+    for (int ih = 0; ih < split_h; ih++)
+        for (int iw = 0; iw < split_w; iw++) {
+            uint8_t *dst = shards[ih * split_w + iw];
+            for (int b = 0; b < B; b++)
+                for (int f = 0; f < F; f++)
+                    for (int h = 0; h < bh; h++)
+                        for (int w = 0; w < bw; w++) {
+                            size_t d = (((size_t)b * F + f) * bh + h) * bw + w;
+                            size_t g = (((size_t)b * F + f) * Hg + (size_t)ih * bh + h) * Wg +
+                                       (size_t)iw * bw + w;
+                            memcpy(dst + d * row_bytes, x + g * row_bytes, row_bytes);
+                        }
+        }
+    return 0;
+}
+
+/* The inverse: every rank's piece goes back to its place in the grid. */
+int oracle_gather_2d(uint8_t **shards, uint8_t *out, int B, int F, int Hg, int Wg, int split_h,
+                     int split_w, size_t row_bytes) {
+    if (split_h < 1 || split_w < 1 || Hg % split_h != 0 || Wg % split_w != 0) return 1;
+    int bh = Hg / split_h, bw = Wg / split_w;
+    for (int ih = 0; ih < split_h; ih++)
+        for (int iw = 0; iw < split_w; iw++) {
+            const uint8_t *src = shards[ih * split_w + iw];
+            for (int b = 0; b < B; b++)
+                for (int f = 0; f < F; f++)
+                    for (int h = 0; h < bh; h++)
+                        for (int w = 0; w < bw; w++) {
+                            size_t d = (((size_t)b * F + f) * bh + h) * bw + w;
+                            size_t g = (((size_t)b * F + f) * Hg + (size_t)ih * bh + h) * Wg +
+                                       (size_t)iw * bw + w;
+                            memcpy(out + g * row_bytes, src + d * row_bytes, row_bytes);
+                        }
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* SM rotation: SM i writes rank i % world_size.  counts[r] = #SMs on rank r. */
 void oracle_sm_rotation_counts(int n_sm, int W, int *counts) {
     for (int r = 0; r < W; r++) counts[r] = 0;

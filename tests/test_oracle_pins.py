@@ -331,3 +331,95 @@ def test_sp_step_equals_unsharded_attention(W, B, T, H, D, user):
         for t in range(T, T_pad):
             np.testing.assert_allclose(oh[:, t], vbar[:, r * Hl:(r + 1) * Hl], rtol=1e-12,
                                        atol=1e-13)
+
+
+# ------------------------------------------------------------------ 2-D spatial split (LongCat-Video CP)
+def _divisor_pairs(W):
+    return [(a, W // a) for a in range(1, W + 1) if W % a == 0]
+
+
+@pytest.mark.parametrize("W", list(range(1, 65)))
+def test_optimal_split_brute_force(W):
+    # closest to a square: no factor pair has a smaller gap; smaller factor first
+    sh, sw = oracle.optimal_split(W)
+    assert sh * sw == W and sh <= sw
+    assert sw - sh == min(abs(a - b) for a, b in _divisor_pairs(W))
+
+
+def test_optimal_split_literal():
+    assert oracle.optimal_split(8) == (2, 4)
+    assert oracle.optimal_split(4) == (2, 2)
+    assert oracle.optimal_split(6) == (2, 3)
+    assert oracle.optimal_split(7) == (1, 7)
+    assert oracle.optimal_split(12) == (3, 4)
+    assert oracle.optimal_split(16) == (4, 4)
+    assert oracle.optimal_split(1) == (1, 1)
+    with pytest.raises(ValueError):
+        oracle.optimal_split(0)
+
+
+@pytest.mark.parametrize("fixture,W,grid", [("tile_2d_F2_H4_W4_W4.txt", 4, (2, 4, 4)),
+                                             ("tile_2d_F1_H4_W6_W6.txt", 6, (1, 4, 6))])
+def test_tile_2d_hand_enumerated(golden_dir, fixture, W, grid):
+    rows = read_golden(os.path.join(golden_dir, fixture))
+    F, Hg, Wg = grid
+    x = np.arange(F * Hg * Wg, dtype=np.int32).reshape(1, F * Hg * Wg, 1)
+    shards = oracle.tile_2d(x, grid, oracle.optimal_split(W))
+    assert [s.reshape(-1).tolist() for s in shards] == rows
+
+
+@pytest.mark.parametrize("B,grid,split,tail", [(1, (1, 1, 12), (1, 4), (3,)), (2, (1, 8, 3), (4, 1), (2, 5)),
+                                                (1, (3, 2, 5), (1, 1), (7,))])
+def test_tile_2d_reduces_to_the_token_range_tile(B, grid, split, tail):
+    # One band of height across a single-row frame, or one piece of width per
+    # band in a single frame, makes every block a contiguous token range: the
+    # 2-D split is then the 1-D tile.  A 1x1 split is the identity.
+    rng = _rng(11)
+    F, Hg, Wg = grid
+    x = rng.integers(0, 60000, size=(B, F * Hg * Wg) + tail, dtype=np.uint16)
+    got = oracle.tile_2d(x, grid, split)
+    want = oracle.tile(x, split[0] * split[1])
+    for g, w in zip(got, want):
+        assert np.array_equal(g, w)
+
+
+@pytest.mark.parametrize("B,grid,W,tail,dt", [(2, (3, 4, 6), 6, (2, 3), np.uint16), (1, (2, 6, 8), 8, (4,), np.float32),
+                                               (3, (1, 3, 5), 1, (1,), np.uint8), (1, (5, 4, 4), 4, (2, 2), np.float64)])
+def test_tile_2d_brute_force_and_round_trip(B, grid, W, tail, dt):
+    rng = _rng(12)
+    F, Hg, Wg = grid
+    x = (rng.standard_normal((B, F * Hg * Wg) + tail) * 100).astype(dt)
+    sh, sw = oracle.optimal_split(W)
+    shards = oracle.tile_2d(x, grid, (sh, sw))
+    bh, bw = Hg // sh, Wg // sw
+    for r, s in enumerate(shards):
+        ih, iw = divmod(r, sw)
+        i = 0
+        for f in range(F):
+            for h in range(bh):
+                for w in range(bw):
+                    t = (f * Hg + ih * bh + h) * Wg + iw * bw + w
+                    assert np.array_equal(s[:, i], x[:, t])
+                    i += 1
+    assert np.array_equal(oracle.gather_2d(shards, grid, (sh, sw)), x)
+
+
+def test_tile_2d_rejects_a_grid_the_split_does_not_divide():
+    x = np.zeros((1, 1 * 5 * 4, 1), dtype=np.uint8)
+    with pytest.raises(oracle.SplitError):
+        oracle.tile_2d(x, (1, 5, 4), (2, 2))
+    with pytest.raises(oracle.SplitError):
+        oracle.gather_2d([x[:, :5]] * 4, (1, 5, 4), (2, 2))
+
+
+def test_sp_step_2d_equals_unsharded_attention():
+    # The 2-D split only permutes the tokens each rank contributes; after the
+    # head exchange every rank still sees every key, so the step is plain
+    # attention up to the order of the key sum.
+    rng = _rng(13)
+    B, grid, H, D, W = 2, (2, 4, 6), 12, 8, 6
+    T = grid[0] * grid[1] * grid[2]
+    q, k, v = (rng.standard_normal((B, T, H, D)).astype(np.float32) for _ in range(3))
+    got = oracle.sp_step_2d(q, k, v, grid, W)
+    want = oracle.attention(q, k, v)
+    assert np.abs(got - want).max() < 1e-12
