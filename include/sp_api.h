@@ -124,6 +124,41 @@ SP_API int sp_tile(const void *x_pad, void *const *shards, int W, int B, int T_p
             sp_stream_t stream);
 
 /* ----------------------------------------------------------------------
+ * 2-D spatial split: an alternative partition for the tile step, after the
+ * LongCat-Video context-parallel page, section 智能张量拆分 (2-D tensor split).
+ * The latent tokens of a batch item form a row-major [F, Hg, Wg] grid
+ * (frames x patch rows x patch columns; T = F*Hg*Wg).  The world size is
+ * factored as split_h x split_w, the factor pair closest to a square with the
+ * smaller factor on height (sp_optimal_split).  Every frame is cut into
+ * split_h bands of Hg/split_h rows and every band into split_w pieces of
+ * Wg/split_w columns; rank r = ih*split_w + iw holds piece (ih, iw) of every
+ * frame, tokens in (frame, row, column) order:
+ *
+ *   shards[ih*split_w + iw][b, (f*bh + h)*bw + w, :] = x[b, (f*Hg + ih*bh + h)*Wg + iw*bw + w, :]
+ *
+ * Every rank then holds Tl = F*bh*bw tokens, so sp_send_recv_heads,
+ * sp_attention and sp_gather_heads run unchanged on these shards (the
+ * attention sees the keys in another order, which changes only the order of
+ * the key sum).
+ */
+
+/* (split_h, split_w) with split_h * split_w = W, split_w - split_h minimal,
+ * split_h <= split_w.  Host only.  SP_ERR_INVALID_ARG for W < 1. */
+SP_API int sp_optimal_split(int W, int *split_h, int *split_w);
+
+/* x [B, F*Hg*Wg, row_bytes] -> shards[r] [B, F*(Hg/split_h)*(Wg/split_w),
+ * row_bytes], r < split_h*split_w <= SP_MAX_RANKS.  SP_ERR_NOT_DIVISIBLE if
+ * Hg % split_h or Wg % split_w is not 0 (the blocks must be uniform, as the
+ * token-range partition requires). */
+SP_API int sp_tile_2d(const void *x, void *const *shards, int B, int F, int Hg, int Wg, int split_h, int split_w,
+                      int64_t row_bytes, sp_stream_t stream);
+
+/* The inverse of sp_tile_2d: every rank's piece back to its place in
+ * out [B, F*Hg*Wg, row_bytes].  Same argument rules. */
+SP_API int sp_gather_2d(const void *const *shards, void *out, int B, int F, int Hg, int Wg, int split_h,
+                        int split_w, int64_t row_bytes, sp_stream_t stream);
+
+/* ----------------------------------------------------------------------
  * 换头 (head exchange), the token x head all-to-all, run as an on-device
  * permutation between the W virtual-rank buffers.
  *

@@ -30,6 +30,7 @@ __all__ = [
     "sp_padded_len", "sp_partition", "sp_pad", "sp_pad_mask", "sp_tile", "sp_send_recv_heads",
     "sp_gather_heads", "sp_send_recv_heads_noalloc", "sp_pad_send_heads", "sp_gather_heads_output",
     "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
+    "sp_optimal_split", "sp_tile_2d", "sp_gather_2d",
     "sp_workspace_status", "sp_sm_rotation_counts", "sp_exchange_grid", "new_workspace", "SPError",
     "SPValueError", "SPStep", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
 ]
@@ -130,6 +131,48 @@ def sp_tile(x_pad: torch.Tensor, shards, stream=None):
     check(lib().sp_tile(x_pad.data_ptr(), ptr_array(shards), W, x_pad.shape[0], x_pad.shape[1],
                         _row_bytes(x_pad), stream_handle(stream)))
     return shards
+
+
+# ---------------------------------------------------------------- 2-D spatial split
+def sp_optimal_split(W: int):
+    """(split_h, split_w): the factor pair of W closest to a square, smaller on height."""
+    sh = ctypes.c_int(0)
+    sw = ctypes.c_int(0)
+    check(lib().sp_optimal_split(W, ctypes.byref(sh), ctypes.byref(sw)))
+    return sh.value, sw.value
+
+
+def _split_2d_shapes(x, shards, grid, split, what):
+    F, Hg, Wg = grid
+    sh, sw = split
+    if len(shards) != sh * sw:
+        raise SPValueError(3, f"{what}: {len(shards)} shards for a {sh}x{sw} split")
+    if x.shape[1] != F * Hg * Wg:
+        raise SPValueError(3, f"{what}: {x.shape[1]} tokens for a {F}x{Hg}x{Wg} grid")
+    if Hg % sh or Wg % sw:
+        raise SPValueError(1, f"{what}: grid {Hg}x{Wg} is not divisible by the split {sh}x{sw}")
+    _same(shards, (x.shape[0], F * (Hg // sh) * (Wg // sw), *x.shape[2:]), x.dtype, "shards")
+
+
+def sp_tile_2d(x: torch.Tensor, shards, grid, split=None, stream=None):
+    """x [B, F*Hg*Wg, ...] -> shards[ih*split_w + iw] [B, F*(Hg/split_h)*(Wg/split_w), ...].
+    ``grid`` = (F, Hg, Wg); ``split`` defaults to sp_optimal_split(len(shards))."""
+    _need_cuda(x, *shards)
+    split = tuple(split) if split is not None else sp_optimal_split(len(shards))
+    _split_2d_shapes(x, shards, grid, split, "sp_tile_2d")
+    check(lib().sp_tile_2d(x.data_ptr(), ptr_array(shards), x.shape[0], *grid, *split, _row_bytes(x),
+                           stream_handle(stream)))
+    return shards
+
+
+def sp_gather_2d(shards, out: torch.Tensor, grid, split=None, stream=None) -> torch.Tensor:
+    """Inverse of sp_tile_2d: shards -> out [B, F*Hg*Wg, ...]."""
+    _need_cuda(out, *shards)
+    split = tuple(split) if split is not None else sp_optimal_split(len(shards))
+    _split_2d_shapes(out, shards, grid, split, "sp_gather_2d")
+    check(lib().sp_gather_2d(ptr_array(shards), out.data_ptr(), out.shape[0], *grid, *split, _row_bytes(out),
+                             stream_handle(stream)))
+    return out
 
 
 # ---------------------------------------------------------------- 换头

@@ -46,6 +46,9 @@ SIGNATURES = {
     "sp_pad_mask": (_I, [_P, _P, _I, _I, _I, _P]),
     "sp_partition": (_I, [_I, _I, _IP, _IP]),
     "sp_tile": (_I, [_P, _PP, _I, _I, _I, _I64, _P]),
+    "sp_optimal_split": (_I, [_I, _IP, _IP]),
+    "sp_tile_2d": (_I, [_P, _PP, _I, _I, _I, _I, _I, _I, _I64, _P]),
+    "sp_gather_2d": (_I, [_PP, _P, _I, _I, _I, _I, _I, _I, _I64, _P]),
     "sp_send_recv_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_gather_heads": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sp_send_recv_heads_noalloc": (_I, [_PP, _PP, _I, _I, _I, _I, _I, _I, _IP, _P]),

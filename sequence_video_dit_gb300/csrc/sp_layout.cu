@@ -110,6 +110,35 @@ struct GatherOutOp {  // shard[r] [B,Tl,rb] -> y [B,T_out,rb]; token g comes fro
     }
 };
 
+// 2-D spatial split of the latent grid (LongCat-Video context parallel):
+// x [B, F, Hg, Wg, rb] <-> shard[ih*sw + iw] [B, F, bh, bw, rb] with
+// bh = Hg / sh, bw = Wg / sw.  Rows enumerate (rank, b, f, h, w) so the shard
+// side is contiguous and the grid side is read or written in runs of bw rows.
+template <bool GATHER>
+struct Split2DOp {
+    uint8_t *grid;  // source (tile) or destination (gather)
+    uint8_t *shard[SP_MAX_RANKS];
+    uint32_t per_rank;  // B * F * bh * bw
+    uint32_t bh, bw, Hg, Wg, sw;
+    int64_t rb;
+    __device__ void row(uint32_t i, const uint8_t *&src, uint8_t *&dst) const {
+        const uint32_t r = i / per_rank, j = i - r * per_rank;
+        const uint32_t jw = j / bw, w = j - jw * bw;
+        const uint32_t bf = jw / bh, h = jw - bf * bh;  // bf = b * F + f
+        const uint32_t ih = r / sw, iw = r - ih * sw;
+        const int64_t g = ((int64_t)bf * Hg + (int64_t)ih * bh + h) * Wg + (int64_t)iw * bw + w;
+        uint8_t *sp = shard[r] + (int64_t)j * rb;
+        uint8_t *gp = grid + g * rb;
+        if (GATHER) {
+            src = sp;
+            dst = gp;
+        } else {
+            src = gp;
+            dst = sp;
+        }
+    }
+};
+
 template <int V, class Op>
 __global__ void __launch_bounds__(256) rows_kernel(Op op, uint32_t nrows, int nvec, int tx_log2) {
     const int tx = 1 << tx_log2;
@@ -425,6 +454,40 @@ static int noalloc_scratch(void **out) {
     return SP_OK;
 }
 
+template <bool GATHER>
+static int launch_split_2d(const void *grid, const void *const *shards, int B, int F, int Hg, int Wg, int sh, int sw,
+                           int64_t row_bytes, cudaStream_t st, const char *what) {
+    if (B < 0 || F < 0 || Hg < 0 || Wg < 0 || row_bytes < 0 || !shards || sh < 1 || sw < 1 ||
+        (int64_t)sh * sw > SP_MAX_RANKS)
+        return set_error(SP_ERR_INVALID_ARG, "%s: bad args (split %dx%d, at most %d ranks)", what, sh, sw,
+                         SP_MAX_RANKS);
+    if (Hg % sh != 0 || Wg % sw != 0)
+        return set_error(SP_ERR_NOT_DIVISIBLE, "%s: grid %dx%d is not divisible by the split %dx%d", what, Hg, Wg,
+                         sh, sw);
+    const int W = sh * sw;
+    const uint64_t rows = (uint64_t)B * F * Hg * Wg;
+    if (rows > 0x7fffffffull) return set_error(SP_ERR_INVALID_ARG, "%s: too many tokens", what);
+    Split2DOp<GATHER> op;
+    memset(&op, 0, sizeof(op));
+    op.grid = (uint8_t *)grid;
+    op.bh = (uint32_t)(Hg / sh);
+    op.bw = (uint32_t)(Wg / sw);
+    op.Hg = (uint32_t)Hg;
+    op.Wg = (uint32_t)Wg;
+    op.sw = (uint32_t)sw;
+    op.per_rank = (uint32_t)(rows / W);
+    op.rb = row_bytes;
+    const bool any = rows > 0 && row_bytes > 0;
+    if (any && !grid) return set_error(SP_ERR_INVALID_ARG, "%s: null grid tensor", what);
+    uint64_t align = (uint64_t)(uintptr_t)grid | (uint64_t)row_bytes;
+    for (int r = 0; r < W; r++) {
+        if (any && !shards[r]) return set_error(SP_ERR_INVALID_ARG, "%s: null shard %d", what, r);
+        op.shard[r] = (uint8_t *)shards[r];
+        align |= (uint64_t)(uintptr_t)shards[r];
+    }
+    return launch_rows(op, rows, row_bytes, vector_width(align), st, what);
+}
+
 }  // namespace sp
 
 using namespace sp;
@@ -527,6 +590,28 @@ int sp_tile(const void *x_pad, void *const *shards, int W, int B, int T_pad, int
         align |= (uint64_t)(uintptr_t)shards[r];
     }
     return launch_rows(op, (uint64_t)B * T_pad, row_bytes, vector_width(align), (cudaStream_t)stream, "sp_tile");
+}
+
+int sp_optimal_split(int W, int *split_h, int *split_w) {
+    if (W < 1 || !split_h || !split_w) return set_error(SP_ERR_INVALID_ARG, "sp_optimal_split: W=%d", W);
+    int a = 1;
+    for (int d = 1; (int64_t)d * d <= W; d++)
+        if (W % d == 0) a = d;
+    *split_h = a;
+    *split_w = W / a;
+    return SP_OK;
+}
+
+int sp_tile_2d(const void *x, void *const *shards, int B, int F, int Hg, int Wg, int split_h, int split_w,
+               int64_t row_bytes, sp_stream_t stream) {
+    return launch_split_2d<false>(x, (const void *const *)shards, B, F, Hg, Wg, split_h, split_w, row_bytes,
+                                  (cudaStream_t)stream, "sp_tile_2d");
+}
+
+int sp_gather_2d(const void *const *shards, void *out, int B, int F, int Hg, int Wg, int split_h, int split_w,
+                 int64_t row_bytes, sp_stream_t stream) {
+    return launch_split_2d<true>(out, shards, B, F, Hg, Wg, split_h, split_w, row_bytes, (cudaStream_t)stream,
+                                 "sp_gather_2d");
 }
 
 int sp_gather_output(const void *const *shards, void *out, int W, int B, int Tl, int T_out,

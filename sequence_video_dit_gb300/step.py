@@ -29,14 +29,22 @@ only allocates buffers and issues library calls on the current stream.
 ``fused=True`` runs the same step with the fused exchange entry points: one
 sp_pad_send_heads per tensor (pad + tile + exchange in one pass, no token-shard
 buffers) and one sp_gather_heads_output (inverse exchange + gather + unpad).
+
+``grid=(F, Hg, Wg)`` partitions the tokens with the 2-D spatial split of the
+LongCat-Video context-parallel page (智能张量拆分) instead of token ranges:
+sp_tile_2d gives rank ih*split_w + iw block (ih, iw) of every frame, the
+exchange and attention run unchanged on those shards, and sp_gather_2d puts
+the output blocks back.  The split must divide the grid, so nothing is padded
+and no mask is needed.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (SP_MASK_FULL, SP_MASK_KEY, new_workspace, sp_attention, sp_attention_workspace_bytes,
-               sp_gather_heads, sp_gather_heads_output, sp_gather_output, sp_pad, sp_pad_mask, sp_pad_send_heads,
-               sp_padded_len, sp_partition, sp_send_recv_heads, sp_tile, SPValueError)
+from . import (SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, new_workspace, sp_attention, sp_attention_workspace_bytes,
+               sp_gather_2d, sp_gather_heads, sp_gather_heads_output, sp_gather_output, sp_optimal_split, sp_pad,
+               sp_pad_mask, sp_pad_send_heads, sp_padded_len, sp_partition, sp_send_recv_heads, sp_tile,
+               sp_tile_2d, SPValueError)
 
 
 class _NullTimer:
@@ -90,10 +98,13 @@ class SPStep:
     q [B,T,H,D] goes through the exchange; k/v [B,Tkv,H,D], every key valid.
     ``mask``: "key" (key-only padding mask) or "user" ((B,T,T) user mask,
     self-attention only).
+    ``grid``: (F, Hg, Wg) with F*Hg*Wg = T selects the 2-D spatial split
+    (self-attention, staged exchange).
     """
 
     def __init__(self, W: int, B: int, T: int, H: int, D: int, dtype=torch.bfloat16, mask: str = "key",
-                 Tq: int | None = None, device=None, fused: bool = False, Tkv: int | None = None):
+                 Tq: int | None = None, device=None, fused: bool = False, Tkv: int | None = None,
+                 grid: tuple | None = None):
         if H % W:
             raise SPValueError(2, f"H={H} is not divisible by W={W}")
         if mask not in ("key", "user"):
@@ -104,6 +115,16 @@ class SPStep:
             raise SPValueError(3, "give Tq (small query) or Tkv (small K/V), not both")
         if Tkv is not None and Tkv < 0:
             raise SPValueError(3, f"Tkv={Tkv} < 0")
+        self.grid = tuple(grid) if grid is not None else None
+        if self.grid is not None:
+            if Tq is not None or Tkv is not None or mask != "key" or fused:
+                raise SPValueError(3, "the 2-D split is built for self-attention with the staged exchange")
+            F, Hg, Wg = self.grid
+            if F * Hg * Wg != T:
+                raise SPValueError(3, f"grid {self.grid} does not hold T={T} tokens")
+            self.split = sp_optimal_split(W)
+            if Hg % self.split[0] or Wg % self.split[1]:
+                raise SPValueError(1, f"grid {Hg}x{Wg} is not divisible by the split {self.split[0]}x{self.split[1]}")
         dev = torch.device(device or "cuda")
         self.W, self.B, self.T, self.H, self.D, self.dtype = W, B, T, H, D, dtype
         self.cross = Tq is not None
@@ -131,8 +152,8 @@ class SPStep:
         else:
             self.out = emp(B, Tq, H, D)
             Tq_att = Tq
-        if self.kv_small:
-            self.mask = None  # every replicated key is valid
+        if self.kv_small or self.grid is not None:
+            self.mask = None  # every key is valid: replicated K/V, or a 2-D split with no padding
         elif mask == "key":
             self.mask = torch.empty(1, 1, self.T_pad, dtype=torch.uint8, device=dev)
         else:
@@ -163,7 +184,7 @@ class SPStep:
                 for n in self.names:
                     sp_pad(src[n], self.xpad[n])
             if self.mask is None:
-                pass  # small replicated K/V: no padding mask
+                pass  # no padded keys: replicated K/V or a 2-D split
             elif self.mask_kind == "key":
                 sp_pad_mask(None, self.mask, self.T)
             else:
@@ -177,12 +198,19 @@ class SPStep:
         else:
             with t("tile"):
                 for n in self.names:
-                    sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
+                    if self.grid is not None:
+                        sp_tile_2d(src[n], self.shards[n], self.grid, self.split)
+                    else:
+                        sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
             with t("send_recv_heads"):
                 for n in self.names:
                     sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
-        kind = SP_MASK_KEY if self.mask_kind == "key" else SP_MASK_FULL
-        mask = None if self.mask is None else (self.mask.view(-1) if kind == SP_MASK_KEY else self.mask)
+        if self.mask is None:
+            kind, mask = SP_MASK_NONE, None
+        elif self.mask_kind == "key":
+            kind, mask = SP_MASK_KEY, self.mask.view(-1)
+        else:
+            kind, mask = SP_MASK_FULL, self.mask
         Hl, D = self.Hl, self.D
         with t("attention"):
             if self.kv_small:
@@ -203,5 +231,8 @@ class SPStep:
                 with t("gather_heads"):
                     sp_gather_heads(self.o_heads, self.o_shards, self.ws_exchange)
                 with t("gather_output"):
-                    sp_gather_output(self.o_shards, out)
+                    if self.grid is not None:
+                        sp_gather_2d(self.o_shards, out, self.grid, self.split)
+                    else:
+                        sp_gather_output(self.o_shards, out)
         return out

@@ -222,3 +222,36 @@ def test_mismatched_rank_buffers_are_rejected_before_launch():
         sp.sp_tile(torch.zeros(B, W * Tl, H, D, device="cuda"), [torch.zeros(B, Tl + 1, H, D, device="cuda")] * W)
     with pytest.raises(ValueError):
         sp.sp_unpad(torch.zeros(B, 8, H, D, device="cuda"), torch.zeros(B, 9, H, D, device="cuda"))
+
+
+@pytest.mark.parametrize("B,grid,W,H,D,dtype", [
+    (1, (16, 24, 16), 8, 32, 128, torch.bfloat16),  # 6144 video tokens, split 2x4, blocks 12x4
+    (2, (3, 4, 6), 6, 6, 8, torch.float32),          # split 2x3
+    (1, (2, 5, 6), 3, 3, 5, torch.bfloat16),         # split 1x3, 30-byte rows: 2-byte vectors
+    (2, (2, 3, 3), 1, 2, 4, torch.float32),          # W = 1: identity
+])
+def test_tile_2d_and_gather_2d_bit_exact(B, grid, W, H, D, dtype):
+    g = torch.Generator().manual_seed(sum(grid) + W)
+    F, Hg, Wg = grid
+    x = random_bytes((B, F * Hg * Wg, H, D), dtype, g)
+    split = sp.sp_optimal_split(W)
+    assert split == oracle.optimal_split(W)
+    Tl = F * (Hg // split[0]) * (Wg // split[1])
+    shards = [torch.empty(B, Tl, H, D, dtype=dtype, device="cuda") for _ in range(W)]
+    sp.sp_tile_2d(x, shards, grid)
+    want = oracle.tile_2d(bytes_np(x), grid, split)
+    for r in range(W):
+        assert np.array_equal(bytes_np(shards[r]), want[r])
+    back = torch.empty_like(x)
+    sp.sp_gather_2d(shards, back, grid)
+    assert np.array_equal(bytes_np(back), oracle.gather_2d(want, grid, split))
+    assert torch.equal(back.view(torch.uint8), x.view(torch.uint8))
+
+
+def test_tile_2d_argument_errors():
+    x = torch.zeros(1, 1 * 5 * 4, 4, 8, dtype=torch.bfloat16, device="cuda")
+    shards = [torch.zeros(1, 5, 4, 8, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    with pytest.raises(ValueError):  # 5 patch rows cannot be cut into 2 bands
+        sp.sp_tile_2d(x, shards, (1, 5, 4))
+    with pytest.raises(ValueError):  # token count does not match the grid
+        sp.sp_tile_2d(x, shards, (1, 4, 4), (2, 2))

@@ -158,3 +158,34 @@ def test_small_kv_cross_attention(W, B, T, Tkv, H, D, dtype, fused):
         rows = _sample_rows(B, T, H, 256, wl.seed)
         ref = oracle.attention_rows(q, k, v, rows)
         assert max_abs(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= tol_for(dtype)
+
+
+@pytest.mark.parametrize("W,B,grid,H,D,dtype,nsample", [
+    (6, 2, (2, 4, 6), 12, 32, torch.float32, None),      # CUDA-core path, every row
+    (8, 1, (16, 24, 16), 32, 128, torch.bfloat16, 384),  # 6144 video tokens, blocks 12x4
+])
+def test_step_with_2d_spatial_split(W, B, grid, H, D, dtype, nsample):
+    # The 2-D split permutes which tokens a rank contributes; after the head
+    # exchange every rank still sees every key, so the step is plain attention.
+    T = grid[0] * grid[1] * grid[2]
+    wl = workloads.make_custom("grid2d", W=W, B=B, T=T, H=H, D=D, dtype="f32" if dtype == torch.float32 else "bf16",
+                               index=300 + W)
+    inp = workloads.make_inputs(wl)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    step = sp.SPStep(W, B, T, H, D, dtype=dtype, grid=grid)
+    out = f32_np(step(dev["q"], dev["k"], dev["v"]))
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    assert sp.sp_workspace_status(step.ws_attn)[0] == 0
+    q, k, v = (inp[n].float().numpy() for n in ("q", "k", "v"))
+    if nsample is None:
+        assert max_abs(out, oracle.attention(q, k, v)) <= tol_for(dtype)
+    else:
+        rows = _sample_rows(B, T, H, nsample, wl.seed)
+        ref = oracle.attention_rows(q, k, v, rows)
+        assert max_abs(out[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= tol_for(dtype)
+
+
+def test_2d_split_rejects_an_indivisible_grid():
+    with pytest.raises(ValueError):
+        sp.SPStep(8, 1, 1 * 5 * 8, 8, 64, grid=(1, 5, 8))  # 5 patch rows, split 2x4

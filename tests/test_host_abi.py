@@ -89,3 +89,13 @@ def test_status_strings(L):
     with pytest.raises(ValueError):
         L.sp_partition(5, 2)
     assert b"not divisible" in lib.sp_last_error()
+
+
+@pytest.mark.parametrize("W", list(range(1, 33)))
+def test_optimal_split_matches_oracle(L, W):
+    assert L.sp_optimal_split(W) == oracle.optimal_split(W)
+
+
+def test_optimal_split_rejects_zero(L):
+    with pytest.raises(ValueError):
+        L.sp_optimal_split(0)
