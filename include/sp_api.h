@@ -79,6 +79,15 @@ typedef enum {
  * caller zero-fills it once; calls leave it ready for the next call. */
 #define SP_WORKSPACE_HEADER_BYTES 256
 
+/* Fault injection for tests of the device-side timeouts (no counterpart in
+ * the pages): the int32 at this byte offset of a workspace is 0 in normal
+ * use.  A positive value k makes the tensor-core attention kernel that uses
+ * the workspace issue only its first k - 1 K/V tile loads, so its bounded
+ * waits run out (2 s each): the call then leaves SP_ERR_TIMEOUT in the
+ * status word, every CTA drains what it had in flight and exits, and the
+ * context stays usable.  Nothing faults and nothing waits without a bound. */
+#define SP_WORKSPACE_KV_STALL_OFFSET 80
+
 /* Human-readable name of a status code (static string). */
 SP_API const char *sp_status_string(int status);
 /* Thread-local message describing the last failing call on this thread. */

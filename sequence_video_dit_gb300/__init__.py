@@ -23,8 +23,9 @@ import math
 import torch
 
 from . import _lib
-from ._lib import (SP_BF16, SP_F32, SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_MAX_RANKS,
-                   SP_WORKSPACE_HEADER_BYTES, SPError, SPValueError, check, lib, ptr_array, stream_handle)
+from ._lib import (SP_BF16, SP_ERR_TIMEOUT, SP_F32, SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_MAX_RANKS,
+                   SP_WORKSPACE_HEADER_BYTES, SP_WORKSPACE_KV_STALL_OFFSET, SPError, SPValueError, check, lib,
+                   ptr_array, stream_handle)
 
 __all__ = [
     "sp_padded_len", "sp_partition", "sp_pad", "sp_pad_mask", "sp_tile", "sp_send_recv_heads",

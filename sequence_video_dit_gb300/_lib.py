@@ -30,6 +30,7 @@ SP_F32, SP_BF16 = 0, 1
 SP_MASK_NONE, SP_MASK_KEY, SP_MASK_FULL = 0, 1, 2
 SP_MAX_RANKS = 8
 SP_WORKSPACE_HEADER_BYTES = 256
+SP_WORKSPACE_KV_STALL_OFFSET = 80  # test hook word of the workspace header
 
 # Symbols declared in include/sp_api.h, with (restype, argtypes).
 _P, _I, _I64, _Z, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float

@@ -69,6 +69,7 @@ struct alignas(128) TcParams {
     float *part_o;    // split partials [item][split][256][D]
     float *part_lse;  // [item][split][256], log2 domain
     int *status;
+    const int *kv_stall;  // workspace test hook (see SP_WORKSPACE_KV_STALL_OFFSET)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -550,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     else tma_load_4d(&bar_q, &p.tq[r], dst, db * 64, h, qp * 256 + i * 128, b);
                 }
             // load n: K of key tile n/2 (n even) or V (n odd) into slot n % NSLOT
-            const int nloads = 2 * nkv;
+            const int stall = *p.kv_stall;  // 0 in normal use
+            const int nloads = stall > 0 ? min(2 * nkv, stall - 1) : 2 * nkv;
             int n = 0;
             for (; n < nloads; n++) {
                 const int slot = n % NSLOT;
@@ -580,8 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                     krow, b);
                 }
             }
-            if (*abort_flag && (!PAIR || leader)) {
-                // drain: the newest load of every slot (older ones were consumed)
+            if (!PAIR || leader) {
+                // Before the CTA may exit, every load it issued has landed: wait
+                // for the newest load of every slot (older ones were consumed
+                // before their slot was reused).  In a normal run the MMA thread
+                // waits for the same phases; after an abort these bounded waits
+                // keep the teardown from freeing shared memory under a copy.
                 wait_drain(&bar_q, 0);
                 for (int slot = 0; slot < NSLOT && slot < n; slot++) {
                     const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
@@ -805,7 +811,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             if (nkv > 0) {
                 have = PAIR ? wait_bounded_cl(&bar_of[i], 0, abort_flag, p.status)
                             : wait_bounded(&bar_of[i], 0, abort_flag, p.status);
-                have = __all_sync(0xffffffffu, have);
+                // the four warps decide together: the store below has a
+                // 128-thread barrier that no warp may reach alone
+                have = named_bar_and(1 + i, 128, have);
                 tc_fence_after();
             }
             if (have) {
@@ -1077,6 +1085,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.mask = a.mask;
     prm.mask_vec4 = (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0) ? 1 : 0;
     prm.status = &a.ws->status;
+    prm.kv_stall = &a.ws->kv_stall;
     const int64_t items = (int64_t)a.W * a.B * a.Hl * sp.n_qpairs;
     const int64_t grid = (int64_t)a.W * a.B * a.Hl * prm.n_qp_grid * sp.n_split;
     if (grid == 0) return SP_OK;

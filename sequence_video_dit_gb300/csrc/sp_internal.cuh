@@ -1,6 +1,7 @@
 // Internal helpers shared by the library's translation units.
 #pragma once
 
+#include <stddef.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -17,9 +18,12 @@ struct WorkspaceHeader {
     int observed[SP_MAX_RANKS];      // counters seen by the last CTA of the last exchange
     int launches;                    // completed exchange launches
     int grid;                        // CTAs of the last exchange launch
-    int reserved[64 - 4 - 2 * SP_MAX_RANKS];
+    int kv_stall;                    // test hook, SP_WORKSPACE_KV_STALL_OFFSET: > 0 stops the
+                                     // attention's K/V loads after kv_stall - 1 of them
+    int reserved[64 - 5 - 2 * SP_MAX_RANKS];
 };
 static_assert(sizeof(WorkspaceHeader) == SP_WORKSPACE_HEADER_BYTES, "header size");
+static_assert(offsetof(WorkspaceHeader, kv_stall) == SP_WORKSPACE_KV_STALL_OFFSET, "stall word offset");
 
 // Thread-local error message; returns `code` for chaining.
 int set_error(int code, const char *fmt, ...);

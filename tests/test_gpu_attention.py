@@ -157,3 +157,29 @@ def test_attention_argument_errors():
         sp.sp_attention(q, q, q, q, sp.new_workspace(), sp.SP_MASK_KEY, None)
     with pytest.raises(ValueError):
         sp.sp_attention(q * 9, q * 9, q * 9, q * 9, sp.new_workspace())  # W = 9 > SP_MAX_RANKS
+
+
+@pytest.mark.parametrize("stall", [1, 4])
+def test_bounded_wait_runs_out_and_the_context_survives(stall):
+    # Fault made through the workspace's test word, nothing on the device
+    # faults: the producer issues only stall - 1 K/V loads (1: none; 4: K0, V0,
+    # K1, so the MMAs of the first key tile are in flight when the wait for V1
+    # runs out).  The kernel must report SP_ERR_TIMEOUT, drain, free its TMEM
+    # and exit; the next call on a cleared workspace must be exact again.
+    W, B, Tq, Tk, Hl, D = 1, 1, 256, 512, 1, 128  # one CTA, four key tiles, no split
+    g = torch.Generator().manual_seed(21)
+    q, k, v = (_mk(W, B, T, Hl, D, torch.bfloat16, g) for T in (Tq, Tk, Tk))
+    o = [torch.empty_like(q[0])]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    word = sp.SP_WORKSPACE_KV_STALL_OFFSET // 4
+    ws.view(torch.int32)[word] = stall
+    sp.sp_attention(q, k, v, o, ws)
+    torch.cuda.synchronize()
+    st, _, _ = sp.sp_workspace_status(ws, clear=True)
+    assert st == sp.SP_ERR_TIMEOUT
+    ws.view(torch.int32)[word] = 0
+    sp.sp_attention(q, k, v, o, ws)
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    ref = oracle.attention(f32_np(q[0]), f32_np(k[0]), f32_np(v[0]))
+    assert max_abs(f32_np(o[0]), ref) <= 2e-2

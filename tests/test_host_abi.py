@@ -99,3 +99,12 @@ def test_optimal_split_matches_oracle(L, W):
 def test_optimal_split_rejects_zero(L):
     with pytest.raises(ValueError):
         L.sp_optimal_split(0)
+
+
+def test_header_constants_match_the_binding():
+    src = open(os.path.join(ROOT, "include", "sp_api.h")).read()
+    from sequence_video_dit_gb300 import _lib
+
+    for name in ("SP_WORKSPACE_HEADER_BYTES", "SP_WORKSPACE_KV_STALL_OFFSET"):
+        m = re.search(rf"#define\s+{name}\s+(\d+)", src)
+        assert m and int(m.group(1)) == getattr(_lib, name)
