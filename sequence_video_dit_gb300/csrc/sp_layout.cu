@@ -55,7 +55,18 @@ __device__ __forceinline__ void copy_row(uint8_t *__restrict__ dst, const uint8_
         d[i + 2 * tx] = a2;
         d[i + 3 * tx] = a3;
     }
-    for (; i < nvec; i += tx) d[i] = s[i];
+    // At most three vectors per lane are left.  Their loads are all issued
+    // before the first store: a 1 KB exchange piece is exactly this tail (two
+    // vectors per lane), and a load-store-load-store order there halves the
+    // loads in flight (measured: 0.77 -> 0.92 of the copy bandwidth at 403 MB).
+    const bool h0 = i < nvec, h1 = i + tx < nvec, h2 = i + 2 * tx < nvec;
+    T a0 = vzero<V>(), a1 = vzero<V>(), a2 = vzero<V>();
+    if (h0) a0 = s[i];
+    if (h1) a1 = s[i + tx];
+    if (h2) a2 = s[i + 2 * tx];
+    if (h0) d[i] = a0;
+    if (h1) d[i + tx] = a1;
+    if (h2) d[i + 2 * tx] = a2;
 }
 
 // ---------------------------------------------------------------- row ops
