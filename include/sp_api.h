@@ -202,8 +202,9 @@ SP_API int sp_gather_heads(const void *const *heads, void *const *shards, int W,
                     int D, int elt_bytes, void *workspace, sp_stream_t stream);
 
 /* The exchange fused with its neighbours on one GPU, where the token shards
- * need not exist (the survey of the pages' follow-up work: pad and tile fused
- * with the send; the inverse exchange fused with gather_output).
+ * need not exist: pad and tile fused with the send, the inverse exchange
+ * fused with gather_output.  Same bytes as the staged calls (sections 补齐,
+ * 切分, 换头, 还原), one pass over the data instead of three.
  *
  * sp_pad_send_heads = sp_pad + sp_tile + sp_send_recv_heads in one pass over
  * the caller's x [B, T, H, D]:

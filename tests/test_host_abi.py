@@ -30,7 +30,7 @@ def _declared_symbols():
     return names
 
 
-def test_header_declares_the_north_star_entry_points():
+def test_header_declares_the_step_entry_points():
     names = _declared_symbols()
     for n in ("sp_pad", "sp_partition", "sp_send_recv_heads", "sp_attention", "sp_gather_heads",
               "sp_gather_output", "sp_unpad"):
