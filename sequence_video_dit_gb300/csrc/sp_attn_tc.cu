@@ -63,6 +63,7 @@ struct alignas(128) TcParams {
     CUtensorMap tk_half[SP_MAX_RANKS];  // 64-key box, for the CTA-pair mode
     int W, B, Tq, Tk, Hl;
     int n_qpairs, n_qp_grid, n_kv, n_split, kv_per_split;
+    int n_full;  // SPLIT launches: work items [0, n_full) run whole, the rest in n_split key pieces
     float scale_log2;
     int mask_kind, mask_vec4;
     const uint8_t *mask;
@@ -483,17 +484,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // work item: blockIdx.x -> (rank, batch, head, key split, query pair), query pair
     // fastest; with MC, n_qp_grid rounds n_qpairs up to even and a surplus CTA
     // (qp == n_qpairs) only helps load K/V for its cluster partner
+    //
+    // SPLIT launches: CTAs [0, n_full) take work items [0, n_full) whole; each
+    // later item (the ones that would otherwise form a last, partial wave, or
+    // every item of a short query sequence) is cut into n_split key ranges
+    // whose partial results attn_merge_kernel combines.  `piece` < 0: whole.
     int bid = blockIdx.x;
-    const int qp = bid % p.n_qp_grid;
-    bid /= p.n_qp_grid;
-    const int split = bid % p.n_split;
-    bid /= p.n_split;
+    int qp, piece = -1;
+    int64_t witem = 0;  // work item, (((r * B + b) * Hl + h) * n_qpairs + qp)
+    if (!SPLIT) {
+        qp = bid % p.n_qp_grid;
+        bid /= p.n_qp_grid;
+    } else {
+        if (bid < p.n_full) {
+            witem = bid;
+        } else {
+            const int u = bid - p.n_full;
+            witem = p.n_full + u / p.n_split;
+            piece = u % p.n_split;
+        }
+        qp = (int)(witem % p.n_qpairs);
+        bid = (int)(witem / p.n_qpairs);
+    }
     const int h = bid % p.Hl;
     bid /= p.Hl;
     const int b = bid % p.B;
     const int r = bid / p.B;
-    const int kv0 = split * p.kv_per_split;
-    const int kv1 = min(p.n_kv, kv0 + p.kv_per_split);
+    const int kv0 = piece < 0 ? 0 : piece * p.kv_per_split;
+    const int kv1 = piece < 0 ? p.n_kv : min(p.n_kv, kv0 + p.kv_per_split);
     const int nkv = max(0, kv1 - kv0);
     // CTAs of one head run in step; starting each query pair at a different key
     // tile spreads their concurrent K/V reads over L2 instead of all CTAs asking
@@ -818,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             if (have) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                if (!SPLIT) {
+                if (!SPLIT || piece < 0) {
                     uint8_t *tile = sgen + C::Q_OFF + i * C::TILE;
 #pragma unroll
                     for (int db = 0; db < C::DB; db++) {
@@ -854,8 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                         bulk_wait_read0();
                     }
                 } else {
-                    const int64_t item = (((int64_t)r * p.B + b) * p.Hl + h) * p.n_qpairs + qp;
-                    const int64_t prow = (item * p.n_split + split) * 256 + i * 128 + row;
+                    const int64_t prow = ((witem - p.n_full) * p.n_split + piece) * 256 + i * 128 + row;
                     float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D);
 #pragma unroll
                     for (int cc = 0; cc < D / 32; cc++) {
@@ -894,25 +911,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 struct MergeParams {
     void *o[SP_MAX_RANKS];
     int64_t os[3];
-    int W, B, Tq, Hl, D, n_qpairs, n_split;
+    int W, B, Tq, Hl, D, n_qpairs, n_split, n_full, n_pieced;
     const float *part_o, *part_lse;
 };
 
 template <int NJ>
 __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
+    // one warp per output row of a pieced work item
     const int lane = threadIdx.x & 31;
     const int64_t rowid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nrows = (int64_t)a.W * a.B * a.Hl * a.Tq;
-    if (rowid >= nrows) return;
-    int64_t t = rowid;
-    const int q = (int)(t % a.Tq);
-    t /= a.Tq;
+    if (rowid >= (int64_t)a.n_pieced * 256) return;
+    const int64_t pi = rowid >> 8;
+    const int row = (int)(rowid & 255);
+    int64_t t = a.n_full + pi;
+    const int qp = (int)(t % a.n_qpairs);
+    t /= a.n_qpairs;
     const int h = (int)(t % a.Hl);
     t /= a.Hl;
     const int b = (int)(t % a.B);
     const int r = (int)(t / a.B);
-    const int64_t item = (((int64_t)r * a.B + b) * a.Hl + h) * a.n_qpairs + q / 256;
-    const int row = q % 256;
+    const int q = qp * 256 + row;
+    if (q >= a.Tq) return;
+    const int64_t item = pi;  // partials are indexed by pieced item
     float L = -INFINITY;
     for (int s = 0; s < a.n_split; s++) L = fmaxf(L, a.part_lse[(item * a.n_split + s) * 256 + row]);
     float acc[NJ];
@@ -964,8 +984,18 @@ static int encode_map(CUtensorMap *m, const void *base, int D, int Hl, int T, in
     return SP_OK;
 }
 
+// Work decomposition.  A work item is one (rank, batch, head, query pair); a
+// CTA holds one SM (225 KB of shared memory), so items run in waves of
+// num_SMs.  Two cases cut items into key pieces (merged by LSE afterwards):
+//  - fewer items than SMs (short query sequences): every item, into enough
+//    pieces to fill the SMs, at least 4 key tiles each;
+//  - a last, partial wave: only its items, into the piece count that finishes
+//    soonest, counting each unit's fixed cost (Q load, epilogue, merge) as
+//    four key tiles; kept only when the whole launch gets 3 % shorter.
 struct SplitPlan {
-    int n_qpairs, n_kv, n_split, kv_per_split;
+    int n_qpairs, n_kv;
+    int n_full, n_pieced;  // items run whole / items cut into n_split pieces
+    int n_split, kv_per_split;
     size_t extra_bytes;
 };
 
@@ -974,16 +1004,49 @@ static SplitPlan plan_split(int W, int B, int Tq, int Tk, int Hl, int D, int num
     s.n_qpairs = (Tq + 255) / 256;
     s.n_kv = (Tk + 127) / 128;
     const int64_t items = (int64_t)W * B * Hl * s.n_qpairs;
+    s.n_full = (int)items;
+    s.n_pieced = 0;
     int ns = 1;
     if (items > 0 && items < num_sms && s.n_kv >= 8) {
         ns = (int)(num_sms / items);
         const int cap = s.n_kv / 4;  // at least 4 key tiles per split
         if (ns > cap) ns = cap;
         if (ns < 1) ns = 1;
+        if (ns > 1) {
+            s.n_full = 0;
+            s.n_pieced = (int)items;
+        }
+    } else if (items > num_sms && s.n_kv >= 8) {
+        const int64_t tail = items % num_sms;
+        const double kFixed = 4.0;  // per-unit cost in key tiles (Q load, epilogue, merge)
+        const double whole = s.n_kv + kFixed;
+        double best = whole;
+        for (int c = 2; c <= 8 && tail > 0; c++) {
+            const int per = (s.n_kv + c - 1) / c;
+            if (per < 4) break;
+            const double cost = (double)((tail * c + num_sms - 1) / num_sms) * (per + kFixed);
+            if (cost < best) {
+                best = cost;
+                ns = c;
+            }
+        }
+        // worth it only if the whole launch gets at least 3 % shorter
+        const double full_waves = (double)(items / num_sms);
+        if (ns > 1 && full_waves * whole + best < 0.97 * (full_waves + 1.0) * whole) {
+            s.n_full = (int)(items - tail);
+            s.n_pieced = (int)tail;
+        } else {
+            ns = 1;
+        }
     }
     s.kv_per_split = s.n_kv > 0 ? (s.n_kv + ns - 1) / ns : 1;
     s.n_split = s.n_kv > 0 ? (s.n_kv + s.kv_per_split - 1) / s.kv_per_split : 1;
-    s.extra_bytes = s.n_split > 1 ? (size_t)items * s.n_split * 256 * (size_t)(D + 1) * sizeof(float) : 0;
+    if (s.n_split <= 1) {
+        s.n_split = 1;
+        s.n_full = (int)items;
+        s.n_pieced = 0;
+    }
+    s.extra_bytes = s.n_pieced > 0 ? (size_t)s.n_pieced * s.n_split * 256 * (size_t)(D + 1) * sizeof(float) : 0;
     return s;
 }
 
@@ -1057,6 +1120,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     if (sp.n_split > 1 && (a.extra == nullptr || a.extra_bytes < sp.extra_bytes)) {
         sp.n_split = 1;
         sp.kv_per_split = sp.n_kv > 0 ? sp.n_kv : 1;
+        sp.n_full = a.W * a.B * a.Hl * sp.n_qpairs;
+        sp.n_pieced = 0;
         sp.extra_bytes = 0;
     }
     prm.W = a.W;
@@ -1080,19 +1145,20 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.n_kv = sp.n_kv;
     prm.n_split = sp.n_split;
     prm.kv_per_split = sp.kv_per_split;
+    prm.n_full = sp.n_full;
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.mask_kind = a.mask_kind;
     prm.mask = a.mask;
     prm.mask_vec4 = (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0) ? 1 : 0;
     prm.status = &a.ws->status;
     prm.kv_stall = &a.ws->kv_stall;
-    const int64_t items = (int64_t)a.W * a.B * a.Hl * sp.n_qpairs;
-    const int64_t grid = (int64_t)a.W * a.B * a.Hl * prm.n_qp_grid * sp.n_split;
+    const int64_t grid = sp.n_split > 1 ? (int64_t)sp.n_full + (int64_t)sp.n_pieced * sp.n_split
+                                        : (int64_t)a.W * a.B * a.Hl * prm.n_qp_grid;
     if (grid == 0) return SP_OK;
     if (grid > 0x7fffffffll) return set_error(SP_ERR_INVALID_ARG, "sp_attention: grid too large");
     if (sp.n_split > 1) {
         prm.part_o = reinterpret_cast<float *>(a.extra);
-        prm.part_lse = prm.part_o + (size_t)items * sp.n_split * 256 * a.D;
+        prm.part_lse = prm.part_o + (size_t)sp.n_pieced * sp.n_split * 256 * a.D;
         rc = (a.D == 64) ? launch_tc_t<64, true, 0>(prm, (unsigned)grid, st)
                          : launch_tc_t<128, true, 0>(prm, (unsigned)grid, st);
         if (rc) return rc;
@@ -1107,9 +1173,11 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         mp.D = a.D;
         mp.n_qpairs = sp.n_qpairs;
         mp.n_split = sp.n_split;
+        mp.n_full = sp.n_full;
+        mp.n_pieced = sp.n_pieced;
         mp.part_o = prm.part_o;
         mp.part_lse = prm.part_lse;
-        const int64_t rows = (int64_t)a.W * a.B * a.Hl * a.Tq;
+        const int64_t rows = (int64_t)sp.n_pieced * 256;
         const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
         if (a.D == 64) tc::attn_merge_kernel<2><<<blocks, 256, 0, st>>>(mp);
         else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);

@@ -17,13 +17,15 @@ SCRIPT = r"""
 import sys, torch
 sys.path.insert(0, sys.argv[1])
 import sequence_video_dit_gb300 as sp
-W, B, T, Hl, D = 4, 1, 1300, 2, 128   # 3 query pairs per head: the last cluster has a surplus CTA
+W, B, T, Hl, D = 4, 1, 1300, 2, 128   # 6 query pairs per head (the last one ragged)
 g = torch.Generator().manual_seed(5)
 mk = lambda: [torch.randn(B, T, Hl, D, generator=g).bfloat16().cuda() for _ in range(W)]
 q, k, v = mk(), mk(), mk()
 o = [torch.full_like(x, float("nan")) for x in q]
 mask = torch.ones(T, dtype=torch.uint8); mask[-7:] = 0
-ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16))
+# A header-only workspace: no key split, so the cluster variants are eligible
+# (split plans always run the single-CTA kernel).
+ws = sp.new_workspace()
 sp.sp_attention(q, k, v, o, ws, sp.SP_MASK_KEY, mask.cuda())
 torch.cuda.synchronize()
 assert sp.sp_workspace_status(ws)[0] == 0
