@@ -492,9 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     int bid = blockIdx.x;
     int qp, piece = -1;
     int64_t witem = 0;  // work item, (((r * B + b) * Hl + h) * n_qpairs + qp)
+    int kv0, kv1;
     if (!SPLIT) {
         qp = bid % p.n_qp_grid;
         bid /= p.n_qp_grid;
+        // (n_split is 1 here; the key range is still derived from the grid,
+        // which keeps this instance's code as it measured fastest)
+        const int split = bid % p.n_split;
+        bid /= p.n_split;
+        kv0 = split * p.kv_per_split;
+        kv1 = min(p.n_kv, kv0 + p.kv_per_split);
     } else {
         if (bid < p.n_full) {
             witem = bid;
@@ -505,13 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
         qp = (int)(witem % p.n_qpairs);
         bid = (int)(witem / p.n_qpairs);
+        kv0 = piece < 0 ? 0 : piece * p.kv_per_split;
+        kv1 = piece < 0 ? p.n_kv : min(p.n_kv, kv0 + p.kv_per_split);
     }
     const int h = bid % p.Hl;
     bid /= p.Hl;
     const int b = bid % p.B;
     const int r = bid / p.B;
-    const int kv0 = piece < 0 ? 0 : piece * p.kv_per_split;
-    const int kv1 = piece < 0 ? p.n_kv : min(p.n_kv, kv0 + p.kv_per_split);
     const int nkv = max(0, kv1 - kv0);
     // CTAs of one head run in step; starting each query pair at a different key
     // tile spreads their concurrent K/V reads over L2 instead of all CTAs asking

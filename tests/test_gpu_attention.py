@@ -183,3 +183,31 @@ def test_bounded_wait_runs_out_and_the_context_survives(stall):
     assert sp.sp_workspace_status(ws)[0] == 0
     ref = oracle.attention(f32_np(q[0]), f32_np(k[0]), f32_np(v[0]))
     assert max_abs(f32_np(o[0]), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("W,B,T,Hl,D", [(8, 1, 3000, 4, 128),   # 384 items: the last 80 run as key pieces
+                                        (8, 2, 2500, 4, 64)])   # 640 items: the last 32 run as key pieces
+def test_last_wave_key_pieces(W, B, T, Hl, D):
+    # With more work items than SMs, the items of the last, partial wave are
+    # cut into key pieces and merged.  Work items are ordered (rank, batch,
+    # head, query pair), so the pieced ones are the last ranks' last heads:
+    # sample rows there and elsewhere against the oracle, per row exactly.
+    g = torch.Generator().manual_seed(T + D)
+    q, k, v = (_mk(W, B, T, Hl, D, torch.bfloat16, g) for _ in range(3))
+    o = [torch.full_like(x, float("nan")) for x in q]
+    mask = torch.ones(T, dtype=torch.uint8)
+    mask[-9:] = 0
+    need = sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16)
+    assert need > sp.SP_WORKSPACE_HEADER_BYTES  # this shape pieces its last wave
+    ws = sp.new_workspace(need)
+    sp.sp_attention(q, k, v, o, ws, sp.SP_MASK_KEY, mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    rng = np.random.default_rng(T)
+    for r in (0, W - 2, W - 1):
+        qs = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 40)]))
+        rows = np.array([(b, int(t), h) for b in range(B) for h in range(Hl) for t in qs], dtype=np.int64)
+        ref = oracle.attention_rows(f32_np(q[r]), f32_np(k[r]), f32_np(v[r]), rows, oracle.MASK_KEY, mask.numpy())
+        got = f32_np(o[r])[rows[:, 0], rows[:, 1], rows[:, 2]]
+        assert np.isfinite(got).all()
+        assert max_abs(got, ref) <= 2e-2, f"rank {r}"
