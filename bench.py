@@ -278,6 +278,8 @@ def run_ours(args, world, rank, local):
     # ---- the same step through the fused exchange entry points (pad + tile +
     # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
     fused = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush)
+    direct = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=True) \
+        if direct_eligible(wl, world) else None
     # ---- end to end: pinned host inputs copied in and the output copied out
     # every step, inside the timed region.  Copies run on their own stream so
     # step i+1's uploads and step i's download overlap step i's compute (two
@@ -309,6 +311,7 @@ def run_ours(args, world, rank, local):
                           "bytes_per_launch": step.exchange_bytes_per_launch()},
         "stage_ms": {k: round(v / stage_n[k], 4) for k, v in stage_ms.items()},
         "fused_step": fused,
+        "direct_step": direct,
         "e2e": {"value": round(weak_scaling_value(flops, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "copies": "pinned host buffers; H2D of step i+1 and D2H of step i overlap step i's compute"},
@@ -329,14 +332,22 @@ def run_ours(args, world, rank, local):
     return result
 
 
-def time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush) -> dict:
-    """Device-resident timing of the step built with ``fused=True`` (same
-    inputs, same output bits), reported beside the staged step."""
+def direct_eligible(wl, world=1) -> bool:
+    """The exchange-free step (attention reading the callers' tensors as token
+    shards) applies when the shards are whole 128-row tiles and need no pad."""
+    return (wl.dtype == "bf16" and wl.D in (64, 128) and wl.T % wl.W == 0 and (wl.T // wl.W) % 128 == 0
+            and wl.mask == "key")
+
+
+def time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=False) -> dict:
+    """Device-resident timing of the step built with ``fused=True`` (and with
+    ``direct=True``: the exchange fused into the attention, in place), same
+    inputs and the same output bits, reported beside the staged step."""
     import sequence_video_dit_gb300 as sp
     from sequence_video_dit_gb300.step import StageTimer
 
     step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, device=dev,
-                     fused=True)
+                     fused=True, direct=direct)
     for _ in range(args.warmup):
         step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
     timer = StageTimer()

@@ -295,6 +295,34 @@ SP_API int sp_attention(const void *const *q, const void *const *k, const void *
                  sp_mask_kind mask_kind, const uint8_t *mask, float scale, void *workspace,
                  size_t workspace_bytes, sp_stream_t stream);
 
+/* The head exchange fused into the attention (one GPU, token shards whose
+ * length is a whole number of 128-row tiles).  sp_send_recv_heads only moves
+ * each rank's heads of every source shard into one buffer; here the
+ * attention's tile loads read them where they are: key tile j (rows
+ * [128j, 128j+128) of the gathered sequence) comes from source shard
+ * s = 128j / (Tk/W), rows 128j - s*(Tk/W), heads [r*Hl, (r+1)*Hl) for rank r.
+ * The masks, the tiles and their order are those of sp_attention on the
+ * exchanged tensors, so the result is the same bit for bit.
+ *
+ * shard_flags: SP_SHARD_KV -- k[s], v[s] are the W source-rank token shards
+ * [B, Tk/W, H, D] (all H heads; strides kv_strides, or NULL for contiguous);
+ * SP_SHARD_Q -- q[s], o[s] are token shards [B, Tq/W, H, D] read and written
+ * in place (o[s] then receives every rank's heads of shard s, the layout
+ * sp_gather_heads produces).  An operand without its flag is per rank as in
+ * sp_attention: [B, T, H/W, D] views with their strides.
+ * H is the total head count (H % W == 0).  A sharded operand needs
+ * T % W == 0 and (T/W) % 128 == 0 (else SP_ERR_NOT_DIVISIBLE /
+ * SP_ERR_UNSUPPORTED: use the exchange); bf16 with D = 64 or 128 only,
+ * 16-byte aligned pointers and strides.  Mask, scale, workspace
+ * (sp_attention_workspace_bytes with Hl = H/W) and status as sp_attention. */
+#define SP_SHARD_KV 1
+#define SP_SHARD_Q 2
+SP_API int sp_attention_shards(const void *const *q, const void *const *k, const void *const *v, void *const *o,
+                               int W, int B, int Tq, int Tk, int H, int D, sp_dtype dtype, int shard_flags,
+                               const int64_t *q_strides, const int64_t *kv_strides, const int64_t *o_strides,
+                               sp_mask_kind mask_kind, const uint8_t *mask, float scale, void *workspace,
+                               size_t workspace_bytes, sp_stream_t stream);
+
 /* Workspace bytes sp_attention wants for this shape on the current device. */
 SP_API size_t sp_attention_workspace_bytes(int W, int B, int Tq, int Tk, int Hl, int D, sp_dtype dtype);
 

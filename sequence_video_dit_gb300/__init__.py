@@ -24,14 +24,14 @@ import torch
 
 from . import _lib
 from ._lib import (SP_BF16, SP_ERR_TIMEOUT, SP_F32, SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_MAX_RANKS,
-                   SP_WORKSPACE_HEADER_BYTES, SP_WORKSPACE_KV_STALL_OFFSET, SPError, SPValueError, check, lib,
-                   ptr_array, stream_handle)
+                   SP_SHARD_KV, SP_SHARD_Q, SP_WORKSPACE_HEADER_BYTES, SP_WORKSPACE_KV_STALL_OFFSET, SPError,
+                   SPValueError, check, lib, ptr_array, stream_handle)
 
 __all__ = [
     "sp_padded_len", "sp_partition", "sp_pad", "sp_pad_mask", "sp_tile", "sp_send_recv_heads",
     "sp_gather_heads", "sp_send_recv_heads_noalloc", "sp_pad_send_heads", "sp_gather_heads_output",
     "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
-    "sp_optimal_split", "sp_tile_2d", "sp_gather_2d",
+    "sp_optimal_split", "sp_tile_2d", "sp_gather_2d", "sp_attention_shards", "SP_SHARD_KV", "SP_SHARD_Q",
     "sp_workspace_status", "sp_sm_rotation_counts", "sp_exchange_grid", "new_workspace", "SPError",
     "SPValueError", "SPStep", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
 ]
@@ -317,6 +317,47 @@ def sp_attention(q, k, v, o, workspace: torch.Tensor, mask_kind: int = SP_MASK_N
 
 
 # ---------------------------------------------------------------- 还原
+def sp_attention_shards(q, k, v, o, workspace: torch.Tensor, shard_flags: int, mask_kind: int = SP_MASK_NONE,
+                        mask=None, scale: float = 0.0, stream=None):
+    """The head exchange fused into the attention: an operand with its flag in
+    ``shard_flags`` is the list of W source-rank token shards [B, T/W, H, D]
+    (views allowed, D contiguous) read -- or for o written -- in place;
+    without it, it is per rank as in sp_attention ([B, T, H/W, D] views)."""
+    W = len(q)
+    if not (len(k) == len(v) == len(o) == W):
+        raise SPValueError(3, "sp_attention_shards: q/k/v/o lists differ in length")
+    for t in (*q, *k, *v, *o):
+        if not t.is_cuda:
+            raise SPValueError(3, "expected CUDA tensors")
+    sq, skv = bool(shard_flags & SP_SHARD_Q), bool(shard_flags & SP_SHARD_KV)
+    B, tq, hq, D = q[0].shape
+    _, tk, hk, _ = k[0].shape
+    H = hq if sq else hq * W
+    if (hk if skv else hk * W) != H:
+        raise SPValueError(3, "sp_attention_shards: q and k disagree on the head count")
+    Tq = tq * W if sq else tq
+    Tk = tk * W if skv else tk
+    for lst, shape in ((q, q[0].shape), (o, q[0].shape), (k, k[0].shape), (v, k[0].shape)):
+        for t in lst:
+            if tuple(t.shape) != tuple(shape) or t.dtype != q[0].dtype or t.stride() != lst[0].stride():
+                raise SPValueError(3, "sp_attention_shards: inconsistent shapes, dtypes or strides")
+    if tuple(k[0].stride()) != tuple(v[0].stride()):
+        raise SPValueError(3, "sp_attention_shards: k and v must share strides")
+    mptr = None
+    if mask_kind != SP_MASK_NONE:
+        if mask is None or not mask.is_cuda or not mask.is_contiguous() or mask.element_size() != 1:
+            raise SPValueError(3, "sp_attention_shards: mask must be a contiguous uint8/bool CUDA tensor")
+        want = Tk if mask_kind == SP_MASK_KEY else B * Tq * Tk
+        if mask.numel() != want:
+            raise SPValueError(3, f"sp_attention_shards: mask has {mask.numel()} elements, expected {want}")
+        mptr = mask.data_ptr()
+    check(lib().sp_attention_shards(ptr_array(q), ptr_array(k), ptr_array(v), ptr_array(o), W, B, Tq, Tk, H, D,
+                                    _dtype_code(q[0].dtype), int(shard_flags), _strides3(q[0]), _strides3(k[0]),
+                                    _strides3(o[0]), mask_kind, mptr, float(scale), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), stream_handle(stream)))
+    return o
+
+
 def sp_gather_output(shards, out: torch.Tensor, stream=None) -> torch.Tensor:
     """shards[r] [B,Tl,...] -> out [B,T_out,...]: each rank's first
     clamp(T_out - r*Tl, 0, Tl) tokens, concatenated."""

@@ -31,6 +31,7 @@ SP_MASK_NONE, SP_MASK_KEY, SP_MASK_FULL = 0, 1, 2
 SP_MAX_RANKS = 8
 SP_WORKSPACE_HEADER_BYTES = 256
 SP_WORKSPACE_KV_STALL_OFFSET = 80  # test hook word of the workspace header
+SP_SHARD_KV, SP_SHARD_Q = 1, 2
 
 # Symbols declared in include/sp_api.h, with (restype, argtypes).
 _P, _I, _I64, _Z, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -60,6 +61,8 @@ SIGNATURES = {
     "sp_exchange_grid": (_I, [_IP]),
     "sp_attention": (_I, [_PP, _PP, _PP, _PP, _I, _I, _I, _I, _I, _I, _I, _I64P, _I64P, _I64P, _I, _P, _F,
                           _P, _Z, _P]),
+    "sp_attention_shards": (_I, [_PP, _PP, _PP, _PP, _I, _I, _I, _I, _I, _I, _I, _I, _I64P, _I64P, _I64P, _I, _P,
+                                 _F, _P, _Z, _P]),
     "sp_attention_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "sp_gather_output": (_I, [_PP, _P, _I, _I, _I, _I, _I64, _P]),
     "sp_unpad": (_I, [_P, _P, _I, _I, _I, _I64, _P]),

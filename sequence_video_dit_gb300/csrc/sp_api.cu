@@ -146,4 +146,72 @@ int sp_attention(const void *const *q, const void *const *k, const void *const *
     return launch_attn_simt(a, st);
 }
 
+int sp_attention_shards(const void *const *q, const void *const *k, const void *const *v, void *const *o, int W,
+                        int B, int Tq, int Tk, int H, int D, sp_dtype dtype, int shard_flags,
+                        const int64_t *q_strides, const int64_t *kv_strides, const int64_t *o_strides,
+                        sp_mask_kind mask_kind, const uint8_t *mask, float scale, void *workspace,
+                        size_t workspace_bytes, sp_stream_t stream) {
+    if (W < 1 || W > SP_MAX_RANKS)
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: W=%d out of [1,%d]", W, SP_MAX_RANKS);
+    if (B < 0 || Tq < 0 || Tk < 0 || H < 1 || D < 1)
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: bad sizes B=%d Tq=%d Tk=%d H=%d D=%d", B, Tq, Tk,
+                         H, D);
+    if (shard_flags & ~(SP_SHARD_Q | SP_SHARD_KV))
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: shard_flags %d", shard_flags);
+    if (H % W != 0)
+        return set_error(SP_ERR_HEADS_NOT_DIVISIBLE, "sp_attention_shards: H=%d is not divisible by W=%d", H, W);
+    const bool sq = (shard_flags & SP_SHARD_Q) != 0, skv = (shard_flags & SP_SHARD_KV) != 0;
+    if ((sq && Tq % W != 0) || (skv && Tk % W != 0))
+        return set_error(SP_ERR_NOT_DIVISIBLE, "sp_attention_shards: total_tokens is not divisible by world_size=%d", W);
+    if ((sq && (Tq / W) % 128 != 0) || (skv && (Tk / W) % 128 != 0))
+        return set_error(SP_ERR_UNSUPPORTED,
+                         "sp_attention_shards: token shards of %d / %d rows are not whole 128-row tiles", sq ? Tq / W : 0,
+                         skv ? Tk / W : 0);
+    if (dtype != SP_BF16 || (D != 64 && D != 128))
+        return set_error(SP_ERR_UNSUPPORTED, "sp_attention_shards: bf16 with D = 64 or 128 only");
+    if (mask_kind != SP_MASK_NONE && mask_kind != SP_MASK_KEY && mask_kind != SP_MASK_FULL)
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: mask_kind %d", (int)mask_kind);
+    if (mask_kind != SP_MASK_NONE && !mask && Tk > 0)
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: mask is NULL");
+    if (!q || !k || !v || !o) return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: null pointer array");
+    if (!workspace || workspace_bytes < SP_WORKSPACE_HEADER_BYTES)
+        return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: workspace must hold >= %d bytes",
+                         SP_WORKSPACE_HEADER_BYTES);
+    if ((uintptr_t)workspace & 15)
+        return set_error(SP_ERR_ALIGNMENT, "sp_attention_shards: workspace not 16-byte aligned");
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.W = W;
+    a.B = B;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.Hl = H / W;
+    a.D = D;
+    a.dtype = dtype;
+    a.q_shard_rows = sq ? Tq / W : 0;
+    a.kv_shard_rows = skv ? Tk / W : 0;
+    default_strides(a.qs, q_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
+    default_strides(a.ks, kv_strides, skv ? Tk / W : Tk, skv ? H : a.Hl, D);
+    default_strides(a.os, o_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
+    for (int r = 0; r < W; r++) {
+        if (!q[r] || !o[r] || (Tk > 0 && (!k[r] || !v[r])))
+            return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: null tensor %d", r);
+        a.q[r] = q[r];
+        a.k[r] = k[r];
+        a.v[r] = v[r];
+        a.o[r] = o[r];
+    }
+    a.mask_kind = mask_kind;
+    a.mask = mask;
+    a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    a.ws = (WorkspaceHeader *)workspace;
+    a.extra = (uint8_t *)workspace + SP_WORKSPACE_HEADER_BYTES;
+    a.extra_bytes = workspace_bytes - SP_WORKSPACE_HEADER_BYTES;
+    if ((int64_t)W * B * a.Hl * Tq == 0) return SP_OK;
+    if (Tk == 0) return set_error(SP_ERR_UNSUPPORTED, "sp_attention_shards: no keys");
+    if (!attn_tc_supported(a))
+        return set_error(SP_ERR_ALIGNMENT, "sp_attention_shards: tensors and strides must be 16-byte aligned");
+    return launch_attn_tc(a, (cudaStream_t)stream);
+}
+
 }  // extern "C"

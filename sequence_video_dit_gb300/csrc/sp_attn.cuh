@@ -13,6 +13,11 @@ struct AttnArgs {
     int W, B, Tq, Tk, Hl, D;
     sp_dtype dtype;
     int64_t qs[3], ks[3], os[3];  // batch, token, head strides in elements
+    // 0: q/o (resp. k/v) are per-rank [B, T, Hl, D] tensors; > 0: they are the
+    // W source-rank token shards [B, shard_rows, W*Hl, D] (rank r's heads at
+    // [r*Hl, (r+1)*Hl)), read and written in place -- the exchange fused into
+    // the attention.  shard_rows is a multiple of the 128-row tile.
+    int q_shard_rows, kv_shard_rows;
     int mask_kind;
     const uint8_t *mask;
     float scale;

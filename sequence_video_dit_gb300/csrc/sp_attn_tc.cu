@@ -64,6 +64,9 @@ struct alignas(128) TcParams {
     int W, B, Tq, Tk, Hl;
     int n_qpairs, n_qp_grid, n_kv, n_split, kv_per_split;
     int n_full;  // SPLIT launches: work items [0, n_full) run whole, the rest in n_split key pieces
+    // > 0: Q/O (resp. K/V) maps are per source token shard of this many rows,
+    // addressed with head r * Hl + h; a 128-row tile never straddles shards
+    int q_shard_rows, kv_shard_rows;
     float scale_log2;
     int mask_kind, mask_vec4;
     const uint8_t *mask;
@@ -452,6 +455,25 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
     }
 }
 
+// Where a 128-row tile starting at global row `row` of rank r's head h lives:
+// the rank's own tensor (shard_rows == 0), or token shard row / shard_rows of
+// the source ranks, at head r * Hl + h.  Rows past the last shard (a ragged
+// query tile) map into the last shard past its end, where TMA loads read
+// zeros and stores are clipped.
+__device__ __forceinline__ void tile_source(int shard_rows, int row, int r, int h, int Hl, int W, int &map,
+                                            int &head, int &srow) {
+    if (shard_rows <= 0) {
+        map = r;
+        head = h;
+        srow = row;
+        return;
+    }
+    const int s = min(row / shard_rows, W - 1);
+    map = s;
+    head = r * Hl + h;
+    srow = row - s * shard_rows;
+}
+
 // ------------------------------------------------------------------ kernel
 // MC: the grid is made of 2-CTA clusters whose CTAs serve adjacent query pairs
 // of the same (rank, batch, head); each CTA loads one 64-column half of every
@@ -569,12 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             // the leader arms for both CTAs' bytes; the partner never arms it
             const uint32_t lq = PAIR ? mapa_rank(smem_u32(&bar_q), 0) : 0u;
             if (!PAIR || leader) mbar_arrive_expect_tx(&bar_q, (PAIR ? 4 : 2) * C::TILE);
-            for (int i = 0; i < 2; i++)
+            for (int i = 0; i < 2; i++) {
+                int qmap, qhead, qrow;
+                tile_source(p.q_shard_rows, qp * 256 + i * 128, r, h, p.Hl, p.W, qmap, qhead, qrow);
                 for (int db = 0; db < C::DB; db++) {
                     const uint32_t dst = sbase + C::Q_OFF + i * C::TILE + db * 16384;
                     if (PAIR) tma_load_4d_pair(lq, &p.tq[r], dst, db * 64, h, qp * 256 + i * 128, b);
-                    else tma_load_4d(&bar_q, &p.tq[r], dst, db * 64, h, qp * 256 + i * 128, b);
+                    else tma_load_4d(&bar_q, &p.tq[qmap], dst, db * 64, qhead, qrow, b);
                 }
+            }
             // load n: K of key tile n/2 (n even) or V (n odd) into slot n % NSLOT
             const int stall = *p.kv_stall;  // 0 in normal use
             const int nloads = stall > 0 ? min(2 * nkv, stall - 1) : 2 * nkv;
@@ -586,7 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                       : wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status)))
                     break;
                 if (!PAIR || leader) mbar_arrive_expect_tx(&bar_full[slot], PAIR ? 2 * SLOT : SLOT);
-                const CUtensorMap *m = (n & 1) ? &p.tv[r] : &p.tk[r];
+                int kmap, khead, kshrow;
+                tile_source(p.kv_shard_rows, key_tile(n >> 1) * 128, r, h, p.Hl, p.W, kmap, khead, kshrow);
+                const CUtensorMap *m = (n & 1) ? &p.tv[kmap] : &p.tk[kmap];
                 const int krow = key_tile(n >> 1) * 128;
                 if (PAIR) {
                     const uint32_t dst = sbase + C::R_OFF + slot * SLOT;
@@ -603,8 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                    krow, b, (uint16_t)0x3);
                 } else {
                     for (int db = 0; db < C::DB; db++)
-                        tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, h,
-                                    krow, b);
+                        tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, khead,
+                                    kshrow, b);
                 }
             }
             if (!PAIR || leader) {
@@ -872,9 +899,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     fence_proxy_async_smem();
                     named_bar_sync(1 + i, 128);
                     if (quarter == 0 && lane == 0) {
+                        int omap, ohead, orow;
+                        tile_source(p.q_shard_rows, qp * 256 + i * 128, r, h, p.Hl, p.W, omap, ohead, orow);
                         for (int db = 0; db < C::DB; db++)
-                            tma_store_4d(&p.to[r], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, h,
-                                         qp * 256 + i * 128, b);
+                            tma_store_4d(&p.to[omap], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, ohead,
+                                         orow, b);
                         bulk_commit();
                         bulk_wait_read0();
                     }
@@ -919,6 +948,7 @@ struct MergeParams {
     void *o[SP_MAX_RANKS];
     int64_t os[3];
     int W, B, Tq, Hl, D, n_qpairs, n_split, n_full, n_pieced;
+    int q_shard_rows;  // > 0: o[s] are token shards (see TcParams)
     const float *part_o, *part_lse;
 };
 
@@ -956,7 +986,13 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16 *O = (__nv_bfloat16 *)a.o[r] + b * a.os[0] + (int64_t)q * a.os[1] + h * a.os[2];
+    int omap = r, ohead = h, orow = q;
+    if (a.q_shard_rows > 0) {
+        omap = q / a.q_shard_rows;
+        ohead = r * a.Hl + h;
+        orow = q - omap * a.q_shard_rows;
+    }
+    __nv_bfloat16 *O = (__nv_bfloat16 *)a.o[omap] + b * a.os[0] + (int64_t)orow * a.os[1] + ohead * a.os[2];
 #pragma unroll
     for (int j = 0; j < NJ; j++) O[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
 }
@@ -1116,13 +1152,18 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     if (di.cc_major != 10) return set_error(SP_ERR_UNSUPPORTED, "tcgen05 path needs a Blackwell (sm_10x) device");
     static thread_local tc::TcParams prm;  // 4+ KB: keep it off the stack
     memset(&prm, 0, sizeof(prm));
+    // per-rank tensors: [B, T, Hl, D]; token shards: [B, shard_rows, W*Hl, D]
+    const int qh = a.q_shard_rows > 0 ? a.W * a.Hl : a.Hl, qt = a.q_shard_rows > 0 ? a.q_shard_rows : a.Tq;
+    const int kh = a.kv_shard_rows > 0 ? a.W * a.Hl : a.Hl, kt = a.kv_shard_rows > 0 ? a.kv_shard_rows : a.Tk;
     for (int r = 0; r < a.W; r++) {
-        if ((rc = tc::encode_map(&prm.tq[r], a.q[r], a.D, a.Hl, a.Tq, a.B, a.qs))) return rc;
-        if ((rc = tc::encode_map(&prm.tk[r], a.k[r], a.D, a.Hl, a.Tk, a.B, a.ks))) return rc;
-        if ((rc = tc::encode_map(&prm.tk_half[r], a.k[r], a.D, a.Hl, a.Tk, a.B, a.ks, 64))) return rc;
-        if ((rc = tc::encode_map(&prm.tv[r], a.v[r], a.D, a.Hl, a.Tk, a.B, a.ks))) return rc;
-        if ((rc = tc::encode_map(&prm.to[r], a.o[r], a.D, a.Hl, a.Tq, a.B, a.os))) return rc;
+        if ((rc = tc::encode_map(&prm.tq[r], a.q[r], a.D, qh, qt, a.B, a.qs))) return rc;
+        if ((rc = tc::encode_map(&prm.tk[r], a.k[r], a.D, kh, kt, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.tk_half[r], a.k[r], a.D, kh, kt, a.B, a.ks, 64))) return rc;
+        if ((rc = tc::encode_map(&prm.tv[r], a.v[r], a.D, kh, kt, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.to[r], a.o[r], a.D, qh, qt, a.B, a.os))) return rc;
     }
+    prm.q_shard_rows = a.q_shard_rows;
+    prm.kv_shard_rows = a.kv_shard_rows;
     tc::SplitPlan sp = tc::plan_split(a.W, a.B, a.Tq, a.Tk, a.Hl, a.D, di.num_sms);
     if (sp.n_split > 1 && (a.extra == nullptr || a.extra_bytes < sp.extra_bytes)) {
         sp.n_split = 1;
@@ -1144,7 +1185,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         const char *e = getenv("SP_ATTN_CLUSTER_MODE");
         return (e && e[0] >= '0' && e[0] <= '2' && e[1] == 0) ? e[0] - '0' : -1;
     }();
-    const bool pairable = a.D == 128 && sp.n_split == 1 && sp.n_qpairs >= 2;
+    const bool pairable = a.D == 128 && sp.n_split == 1 && sp.n_qpairs >= 2 && a.q_shard_rows == 0 &&
+                          a.kv_shard_rows == 0;
     const int mode = pairable ? (mode_env >= 0 ? mode_env : 0) : 0;
     const bool mc = mode != 0;
     prm.n_qpairs = sp.n_qpairs;
@@ -1182,6 +1224,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         mp.n_split = sp.n_split;
         mp.n_full = sp.n_full;
         mp.n_pieced = sp.n_pieced;
+        mp.q_shard_rows = a.q_shard_rows;
         mp.part_o = prm.part_o;
         mp.part_lse = prm.part_lse;
         const int64_t rows = (int64_t)sp.n_pieced * 256;

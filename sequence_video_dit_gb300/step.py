@@ -36,12 +36,23 @@ sp_tile_2d gives rank ih*split_w + iw block (ih, iw) of every frame, the
 exchange and attention run unchanged on those shards, and sp_gather_2d puts
 the output blocks back.  The split must divide the grid, so nothing is padded
 and no mask is needed.
+
+``direct=True`` fuses the head exchange into the attention
+(sp_attention_shards): the operands that would go through sp_send_recv_heads
+are handed over as the W token shards and each attention tile is loaded from
+its source shard, O is written into token-shard layout, so no exchange kernel
+runs.  It needs shards of whole 128-row tiles (T_pad / W a multiple of 128)
+and the tensor-core kernel (bf16, D = 64 or 128).  With ``fused=False`` the
+shards are the W rank buffers sp_tile (or sp_tile_2d) fills and
+sp_gather_output (sp_gather_2d) assembles the output; with ``fused=True`` they
+are views of the caller's tensors and nothing is copied at all (T % W == 0).
+Either way the output equals the staged step's bit for bit.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, new_workspace, sp_attention, sp_attention_workspace_bytes,
+from . import (SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_SHARD_KV, SP_SHARD_Q, new_workspace, sp_attention_shards, sp_attention, sp_attention_workspace_bytes,
                sp_gather_2d, sp_gather_heads, sp_gather_heads_output, sp_gather_output, sp_optimal_split, sp_pad,
                sp_pad_mask, sp_pad_send_heads, sp_padded_len, sp_partition, sp_send_recv_heads, sp_tile,
                sp_tile_2d, SPValueError)
@@ -100,11 +111,12 @@ class SPStep:
     self-attention only).
     ``grid``: (F, Hg, Wg) with F*Hg*Wg = T selects the 2-D spatial split
     (self-attention, staged exchange).
+    ``direct``: the exchange fused into the attention (see the module text).
     """
 
     def __init__(self, W: int, B: int, T: int, H: int, D: int, dtype=torch.bfloat16, mask: str = "key",
                  Tq: int | None = None, device=None, fused: bool = False, Tkv: int | None = None,
-                 grid: tuple | None = None):
+                 grid: tuple | None = None, direct: bool = False):
         if H % W:
             raise SPValueError(2, f"H={H} is not divisible by W={W}")
         if mask not in ("key", "user"):
@@ -138,15 +150,26 @@ class SPStep:
         self.Hl = H // W
         self.need_pad = self.T_pad != T
         self.fused = fused
+        self.direct = direct
+        if direct:
+            if dtype != torch.bfloat16 or D not in (64, 128):
+                raise SPValueError(6, "direct: the tensor-core attention needs bf16 and D = 64 or 128")
+            if self.Tl % 128:
+                raise SPValueError(6, f"direct: token shards of {self.Tl} rows are not whole 128-row tiles")
+            if fused and self.need_pad:
+                raise SPValueError(1, f"direct + fused reads the caller's tensors in place: T={T} % W={W} != 0")
+        # shard views of the caller's tensors (direct + fused) need no buffers
+        views = direct and fused
         names = ("k", "v") if self.cross else (("q",) if self.kv_small else ("q", "k", "v"))
         self.names = names
         emp = lambda *shape: torch.empty(*shape, dtype=dtype, device=dev)  # noqa: E731
         self.xpad = {n: emp(B, self.T_pad, H, D) for n in names} if (self.need_pad and not fused) else {}
-        self.shards = {} if fused else {n: [emp(B, self.Tl, H, D) for _ in range(W)] for n in names}
-        self.heads = {n: [emp(B, self.T_pad, self.Hl, D) for _ in range(W)] for n in names}
+        self.shards = {} if (fused and not direct) or views else {n: [emp(B, self.Tl, H, D) for _ in range(W)]
+                                                                   for n in names}
+        self.heads = {} if direct else {n: [emp(B, self.T_pad, self.Hl, D) for _ in range(W)] for n in names}
         if not self.cross:
-            self.o_heads = [emp(B, self.T_pad, self.Hl, D) for _ in range(W)]
-            self.o_shards = [] if fused else [emp(B, self.Tl, H, D) for _ in range(W)]
+            self.o_heads = [] if direct else [emp(B, self.T_pad, self.Hl, D) for _ in range(W)]
+            self.o_shards = [] if (fused and not direct) or views else [emp(B, self.Tl, H, D) for _ in range(W)]
             self.out = emp(B, T, H, D)
             Tq_att = self.T_pad
         else:
@@ -168,7 +191,13 @@ class SPStep:
 
     def n_exchange_launches(self) -> int:
         """Launches of the exchange kernels per step (send per tensor + gather)."""
+        if self.direct:
+            return 0
         return len(self.names) + (0 if self.cross else 1)
+
+    def _shard_views(self, x):
+        """The W token shards of a caller tensor [B, T, H, D] as views (T % W == 0)."""
+        return [x[:, s * self.Tl:(s + 1) * self.Tl] for s in range(self.W)]
 
     def __call__(self, q, k, v, user_mask=None, timer=None, out=None):
         """Runs the step on the current stream and returns the output tensor
@@ -191,6 +220,8 @@ class SPStep:
                 if user_mask is None:
                     raise SPValueError(3, "this step was built for a user mask")
                 sp_pad_mask(user_mask, self.mask, self.T)
+        if self.direct:
+            return self._direct(q, k, v, src, out, t)
         if self.fused:
             with t("send_recv_heads"):
                 for n in self.names:
@@ -205,12 +236,7 @@ class SPStep:
             with t("send_recv_heads"):
                 for n in self.names:
                     sp_send_recv_heads(self.shards[n], self.heads[n], self.ws_exchange)
-        if self.mask is None:
-            kind, mask = SP_MASK_NONE, None
-        elif self.mask_kind == "key":
-            kind, mask = SP_MASK_KEY, self.mask.view(-1)
-        else:
-            kind, mask = SP_MASK_FULL, self.mask
+        kind, mask = self._mask_arg()
         Hl, D = self.Hl, self.D
         with t("attention"):
             if self.kv_small:
@@ -235,4 +261,47 @@ class SPStep:
                         sp_gather_2d(self.o_shards, out, self.grid, self.split)
                     else:
                         sp_gather_output(self.o_shards, out)
+        return out
+
+    def _mask_arg(self):
+        if self.mask is None:
+            return SP_MASK_NONE, None
+        if self.mask_kind == "key":
+            return SP_MASK_KEY, self.mask.view(-1)
+        return SP_MASK_FULL, self.mask
+
+    def _direct(self, q, k, v, src, out, t):
+        """The step with the exchange fused into the attention: token shards in,
+        O in token-shard layout out (after pad and mask, which ran already)."""
+        W, Hl = self.W, self.Hl
+        if self.fused:  # the caller's tensors, in place
+            shards = {n: self._shard_views(src[n]) for n in self.names}
+            o_sh = None if self.cross else self._shard_views(out)
+        else:
+            with t("tile"):
+                for n in self.names:
+                    if self.grid is not None:
+                        sp_tile_2d(src[n], self.shards[n], self.grid, self.split)
+                    else:
+                        sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
+            shards, o_sh = self.shards, (None if self.cross else self.o_shards)
+        kind, mask = self._mask_arg()
+        with t("attention"):
+            if self.kv_small:
+                kv = [(k[:, :, r * Hl:(r + 1) * Hl, :], v[:, :, r * Hl:(r + 1) * Hl, :]) for r in range(W)]
+                sp_attention_shards(shards["q"], [a for a, _ in kv], [b for _, b in kv], o_sh, self.ws_attn,
+                                    SP_SHARD_Q)
+            elif not self.cross:
+                sp_attention_shards(shards["q"], shards["k"], shards["v"], o_sh, self.ws_attn,
+                                    SP_SHARD_Q | SP_SHARD_KV, kind, mask)
+            else:
+                qv = [q[:, :, r * Hl:(r + 1) * Hl, :] for r in range(W)]
+                ov = [out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(W)]
+                sp_attention_shards(qv, shards["k"], shards["v"], ov, self.ws_attn, SP_SHARD_KV, kind, mask)
+        if not self.cross and not self.fused:
+            with t("gather_output"):
+                if self.grid is not None:
+                    sp_gather_2d(o_sh, out, self.grid, self.split)
+                else:
+                    sp_gather_output(o_sh, out)
         return out

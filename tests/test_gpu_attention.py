@@ -211,3 +211,70 @@ def test_last_wave_key_pieces(W, B, T, Hl, D):
         got = f32_np(o[r])[rows[:, 0], rows[:, 1], rows[:, 2]]
         assert np.isfinite(got).all()
         assert max_abs(got, ref) <= 2e-2, f"rank {r}"
+
+
+@pytest.mark.parametrize("W,B,Tl,H,D,mask_kind", [
+    (8, 1, 384, 32, 128, sp.SP_MASK_KEY),   # c4-like K/V shards, a query pair straddles two shards
+    (4, 2, 256, 8, 64, sp.SP_MASK_FULL),    # user-mask kind, D = 64
+    (2, 1, 128, 4, 128, sp.SP_MASK_NONE),   # one tile per shard
+    (8, 1, 768, 32, 128, sp.SP_MASK_KEY),   # the 6144-token video: the last wave runs in key pieces
+])
+def test_attention_from_shards_is_the_attention_after_the_exchange(W, B, Tl, H, D, mask_kind):
+    # The exchange fused into the attention: loading each tile from its source
+    # shard must give exactly the bytes of sp_send_recv_heads + sp_attention
+    # (+ sp_gather_heads for O in token-shard layout).
+    g = torch.Generator().manual_seed(Tl + W)
+    T = W * Tl
+    mk = lambda: [torch.randn(B, Tl, H, D, generator=g).bfloat16().cuda() for _ in range(W)]  # noqa: E731
+    qs, ks, vs = mk(), mk(), mk()
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = (torch.rand(T, generator=g) < 0.9).to(torch.uint8)
+        mask[0] = 1
+        mask = mask.cuda()
+    elif mask_kind == sp.SP_MASK_FULL:
+        mask = (torch.rand(B, T, T, generator=g) < 0.3).to(torch.uint8)
+        for b in range(B):
+            mask[b, torch.arange(T), torch.arange(T)] = 1
+        mask = mask.cuda()
+    Hl = H // W
+    wx = sp.new_workspace()
+    heads = {}
+    for n, x in (("q", qs), ("k", ks), ("v", vs)):
+        heads[n] = [torch.empty(B, T, Hl, D, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+        sp.sp_send_recv_heads(x, heads[n], wx)
+    o_heads = [torch.empty_like(x) for x in heads["q"]]
+    need = sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16)
+    sp.sp_attention(heads["q"], heads["k"], heads["v"], o_heads, sp.new_workspace(need), mask_kind, mask)
+    o_ref = [torch.empty_like(x) for x in qs]
+    sp.sp_gather_heads(o_heads, o_ref, wx)
+    # everything from / to token shards
+    o_sh = [torch.full_like(x, float("nan")) for x in qs]
+    ws = sp.new_workspace(need)
+    sp.sp_attention_shards(qs, ks, vs, o_sh, ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV, mask_kind, mask)
+    # K/V from shards only; Q and O per rank
+    o_kv = [torch.full_like(x, float("nan")) for x in heads["q"]]
+    sp.sp_attention_shards(heads["q"], ks, vs, o_kv, sp.new_workspace(need), sp.SP_SHARD_KV, mask_kind, mask)
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    for s in range(W):
+        assert torch.equal(o_sh[s].view(torch.int16), o_ref[s].view(torch.int16)), f"shard {s}"
+        assert torch.equal(o_kv[s].view(torch.int16), o_heads[s].view(torch.int16)), f"rank {s}"
+    # and the values are attention: a few rows of rank 0 against the oracle
+    rows = np.array([(0, 0, 0), (0, T - 1, Hl - 1), (B - 1, T // 2, 0)], dtype=np.int64)
+    ref = oracle.attention_rows(f32_np(heads["q"][0]), f32_np(heads["k"][0]), f32_np(heads["v"][0]), rows,
+                                mask_kind, None if mask is None else mask.cpu().numpy())
+    got = f32_np(o_heads[0])[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert max_abs(got, ref) <= 2e-2
+
+
+def test_attention_from_shards_refuses_what_it_cannot_do():
+    W, B, H, D = 4, 1, 8, 128
+    ws = sp.new_workspace()
+    mk = lambda Tl, dt=torch.bfloat16: [torch.zeros(B, Tl, H, D, dtype=dt, device="cuda") for _ in range(W)]  # noqa
+    with pytest.raises(ValueError):  # shards of 100 rows are not whole 128-row tiles
+        x = mk(100)
+        sp.sp_attention_shards(x, x, x, mk(100), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV)
+    with pytest.raises(ValueError):  # no tensor-core kernel for fp32
+        x = mk(128, torch.float32)
+        sp.sp_attention_shards(x, x, x, mk(128, torch.float32), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV)

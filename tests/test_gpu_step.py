@@ -189,3 +189,46 @@ def test_step_with_2d_spatial_split(W, B, grid, H, D, dtype, nsample):
 def test_2d_split_rejects_an_indivisible_grid():
     with pytest.raises(ValueError):
         sp.SPStep(8, 1, 1 * 5 * 8, 8, 64, grid=(1, 5, 8))  # 5 patch rows, split 2x4
+
+
+def _direct_cases():
+    c4 = workloads.get("c4")
+    video = workloads.make_custom("video6144", W=8, B=1, T=6144, H=32, D=128, index=400)
+    padded = workloads.make_custom("video6140", W=8, B=1, T=6140, H=32, D=128, index=401)
+    return [
+        ("c4", c4, dict(Tq=c4.Tq), True),
+        ("video6144", video, {}, True),
+        ("video6140-padded", padded, {}, False),
+        ("video6144-audio1001", workloads.make_custom("a2v", W=8, B=1, T=1001, H=32, D=128, Tq=6144, index=402),
+         "kv_small", True),
+        ("grid16x24x16", video, dict(grid=(16, 24, 16)), False),
+    ]
+
+
+@pytest.mark.parametrize("case", range(5))
+@pytest.mark.parametrize("fused", [False, True])
+def test_direct_step_equals_staged_step_bitwise(case, fused):
+    name, wl, kw, fusable = _direct_cases()[case]
+    if fused and not fusable:
+        pytest.skip("in-place shards need T % W == 0 and contiguous token ranges")
+    inp = workloads.make_inputs(wl)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
+    if kw == "kv_small":  # the workload's query is the sharded video, its T the audio keys
+        T, kw = wl.q_len, dict(Tkv=wl.T)
+    else:
+        T = wl.T
+    staged = sp.SPStep(wl.W, wl.B, T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, **kw)
+    direct = sp.SPStep(wl.W, wl.B, T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, direct=True, fused=fused, **kw)
+    a = staged(dev["q"], dev["k"], dev["v"]).clone()
+    b = direct(dev["q"], dev["k"], dev["v"]).clone()
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(direct.ws_attn)[0] == 0
+    assert direct.n_exchange_launches() == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
+
+
+def test_direct_step_refuses_unaligned_shards():
+    with pytest.raises(ValueError):  # c2: 1004 / 4 = 251-token shards
+        sp.SPStep(4, 2, 1001, 8, 64, mask="user", direct=True)
+    with pytest.raises(ValueError):  # padding cannot happen in place
+        sp.SPStep(8, 1, 6140, 32, 128, direct=True, fused=True)
