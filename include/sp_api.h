@@ -7,7 +7,10 @@
  * (LTX-2 sequence-parallel breakdown):
  *   补齐 (pad)          sp_pad, sp_pad_mask
  *   切分 (partition)    sp_partition, sp_tile
- *   换头 (head swap)    sp_send_recv_heads, sp_attention, sp_gather_heads
+ *   换头 (head swap)    sp_send_recv_heads, sp_attention, sp_gather_heads;
+ *                       sp_attention_shards (the exchange fused into the
+ *                       attention); sp_pad_send_heads / sp_gather_heads_output
+ *                       (the exchange fused with its neighbours)
  *   还原 (restore)      sp_gather_output, sp_unpad
  * and the kernel paragraphs on SM rotation ("SM 轮转") and the completion
  * barrier ("barrier").

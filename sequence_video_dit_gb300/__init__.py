@@ -13,6 +13,9 @@ Stages (after "LTX-2 序列并行拆解"):
   切分  sp_partition, sp_tile
   换头  sp_send_recv_heads, sp_attention, sp_gather_heads
   还原  sp_gather_output, sp_unpad
+Fused forms: sp_pad_send_heads and sp_gather_heads_output (the exchange with
+its neighbours), sp_attention_shards (the exchange inside the attention).
+Alternative partition: sp_optimal_split, sp_tile_2d, sp_gather_2d.
 ``SPStep`` runs the whole step on preallocated buffers.
 """
 from __future__ import annotations
