@@ -280,6 +280,7 @@ def run_ours(args, world, rank, local):
     fused = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush)
     direct = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=True) \
         if direct_eligible(wl, world) else None
+    graphed = time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush)
     # ---- end to end: pinned host inputs copied in and the output copied out
     # every step, inside the timed region.  Copies run on their own stream so
     # step i+1's uploads and step i's download overlap step i's compute (two
@@ -312,6 +313,7 @@ def run_ours(args, world, rank, local):
         "stage_ms": {k: round(v / stage_n[k], 4) for k, v in stage_ms.items()},
         "fused_step": fused,
         "direct_step": direct,
+        "graph_step": graphed,
         "e2e": {"value": round(weak_scaling_value(flops, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "copies": "pinned host buffers; H2D of step i+1 and D2H of step i overlap step i's compute"},
@@ -375,6 +377,35 @@ def time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, 
     del step
     torch.cuda.empty_cache()
     return out
+
+
+def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> dict:
+    """The staged step captured once as a CUDA graph and replayed: the same
+    kernels with one host launch per step (what latency-bound shapes gain)."""
+    import sequence_video_dit_gb300 as sp
+
+    n0 = sp.lib().sp_launch_count()
+    step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
+    per_step = int(sp.lib().sp_launch_count() - n0)
+    g = step.capture(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
+    for _ in range(args.warmup):
+        g.replay()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if not big_inputs:
+            flush.zero_()
+        starts[i].record()
+        g.replay()
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
+    del g
+    return {"value": round(weak_scaling_value(flops, world, ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "kernels_per_replay": per_step}
 
 
 def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev) -> float:

@@ -36,7 +36,7 @@ __all__ = [
     "sp_attention", "sp_attention_workspace_bytes", "sp_gather_output", "sp_unpad",
     "sp_optimal_split", "sp_tile_2d", "sp_gather_2d", "sp_attention_shards", "SP_SHARD_KV", "SP_SHARD_Q",
     "sp_workspace_status", "sp_sm_rotation_counts", "sp_exchange_grid", "new_workspace", "SPError",
-    "SPValueError", "SPStep", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
+    "SPValueError", "SPStep", "StepGraph", "SP_MASK_NONE", "SP_MASK_KEY", "SP_MASK_FULL", "SP_MAX_RANKS", "lib",
 ]
 
 
@@ -385,4 +385,4 @@ def sp_unpad(x_pad: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tenso
     return out
 
 
-from .step import SPStep  # noqa: E402
+from .step import SPStep, StepGraph  # noqa: E402

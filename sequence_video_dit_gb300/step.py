@@ -263,6 +263,22 @@ class SPStep:
                         sp_gather_output(self.o_shards, out)
         return out
 
+    def capture(self, q, k, v, user_mask=None, out=None) -> "StepGraph":
+        """Records the whole step, for these input and output buffers, as one
+        CUDA graph (after one eager run that does the host-side first-call
+        set-up).  ``StepGraph.replay()`` then runs every kernel of the step
+        with a single launch from the host; copy new data into q, k, v (and
+        the user mask) in place between replays."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self(q, k, v, user_mask=user_mask, out=out)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            result = self(q, k, v, user_mask=user_mask, out=out)
+        return StepGraph(graph, result, (q, k, v, user_mask))
+
     def _mask_arg(self):
         if self.mask is None:
             return SP_MASK_NONE, None
@@ -305,3 +321,17 @@ class SPStep:
                 else:
                     sp_gather_output(o_sh, out)
         return out
+
+
+class StepGraph:
+    """A captured SP step: ``replay()`` reruns it on the captured buffers and
+    returns the output tensor (the same storage every time)."""
+
+    def __init__(self, graph, out, inputs):
+        self.graph = graph
+        self.out = out
+        self._inputs = inputs  # kept alive: the graph reads them by address
+
+    def replay(self):
+        self.graph.replay()
+        return self.out

@@ -232,3 +232,28 @@ def test_direct_step_refuses_unaligned_shards():
         sp.SPStep(4, 2, 1001, 8, 64, mask="user", direct=True)
     with pytest.raises(ValueError):  # padding cannot happen in place
         sp.SPStep(8, 1, 6140, 32, 128, direct=True, fused=True)
+
+
+@pytest.mark.parametrize("name,kw", [("c1", {}), ("c2", {}), ("c3", {}), ("c3", dict(fused=True)),
+                                     ("c4", dict(fused=True, direct=True))])
+def test_captured_step_replays_the_eager_step_bitwise(name, kw):
+    # The whole step as one CUDA graph: same bytes as the eager step, on the
+    # captured inputs and again after new inputs are copied into them.
+    wl = workloads.get(name)
+    inp, dev, um = _inputs(wl)
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, **kw)
+    eager = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, **kw)
+    g = step.capture(dev["q"], dev["k"], dev["v"], user_mask=um)
+    a = g.replay().clone()
+    b = eager(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    new = workloads.make_inputs(wl, seed=wl.seed + 77)
+    for n in ("q", "k", "v"):
+        dev[n].copy_(new[n])
+    a = g.replay().clone()
+    b = eager(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    assert sp.sp_workspace_status(step.ws_attn)[0] == 0
