@@ -13,7 +13,9 @@
  *                       (the exchange fused with its neighbours)
  *   还原 (restore)      sp_gather_output, sp_unpad
  * and the kernel paragraphs on SM rotation ("SM 轮转") and the completion
- * barrier ("barrier").
+ * barrier ("barrier").  An alternative partition for the tile step follows
+ * the LongCat-Video context-parallel page (智能张量拆分, 2-D tensor split):
+ * sp_optimal_split, sp_tile_2d, sp_gather_2d.
  *
  * Conventions shared by every entry point
  *   - Activations are row-major [B, T, H, D] ("tokens x heads x head_dim").
