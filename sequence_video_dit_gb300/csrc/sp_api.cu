@@ -124,6 +124,7 @@ int sp_attention(const void *const *q, const void *const *k, const void *const *
     default_strides(a.ks, kv_strides, Tk, Hl, D);
     default_strides(a.os, o_strides, Tq, Hl, D);
     const size_t elt = dtype == SP_F32 ? 4 : 2;
+    if ((int64_t)W * B * Hl * Tq == 0) return SP_OK;  // nothing to compute (empty tensors may be null)
     for (int r = 0; r < W; r++) {
         if (!q[r] || !o[r] || (Tk > 0 && (!k[r] || !v[r])))
             return set_error(SP_ERR_INVALID_ARG, "sp_attention: null tensor for rank %d", r);
@@ -193,6 +194,7 @@ int sp_attention_shards(const void *const *q, const void *const *k, const void *
     default_strides(a.qs, q_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
     default_strides(a.ks, kv_strides, skv ? Tk / W : Tk, skv ? H : a.Hl, D);
     default_strides(a.os, o_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
+    if ((int64_t)W * B * (H / W) * Tq == 0) return SP_OK;  // nothing to compute (empty tensors may be null)
     for (int r = 0; r < W; r++) {
         if (!q[r] || !o[r] || (Tk > 0 && (!k[r] || !v[r])))
             return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: null tensor %d", r);

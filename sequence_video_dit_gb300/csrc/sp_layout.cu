@@ -404,8 +404,9 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
     p.chunk_bytes = (int64_t)Hl * D * elt;
     p.row_bytes = (int64_t)H * D * elt;
     align |= (uint64_t)p.chunk_bytes;
+    const bool any = (int64_t)B * Tl > 0;  // empty tensors may carry null pointers
     for (int i = 0; i < W; i++) {
-        if (!src[i] || !dst[i]) return set_error(SP_ERR_INVALID_ARG, "%s: null buffer for rank %d", what, i);
+        if (any && (!src[i] || !dst[i])) return set_error(SP_ERR_INVALID_ARG, "%s: null buffer for rank %d", what, i);
         p.src[i] = (const uint8_t *)src[i];
         p.dst[i] = (uint8_t *)dst[i];
         align |= (uint64_t)(uintptr_t)src[i] | (uint64_t)(uintptr_t)dst[i];
@@ -558,8 +559,9 @@ int sp_unpad(const void *x_pad, void *out, int B, int T_pad, int T, int64_t row_
 }
 
 int sp_pad_mask(const uint8_t *user_mask, uint8_t *mask_out, int B, int T, int T_pad, sp_stream_t stream) {
-    if (B < 0 || T < 0 || T_pad < T || !mask_out) return set_error(SP_ERR_INVALID_ARG, "sp_pad_mask: bad args");
-    if (T_pad == 0) return SP_OK;
+    if (B < 0 || T < 0 || T_pad < T) return set_error(SP_ERR_INVALID_ARG, "sp_pad_mask: bad args");
+    if (T_pad == 0 || (user_mask && B == 0)) return SP_OK;  // empty masks may carry null pointers
+    if (!mask_out) return set_error(SP_ERR_INVALID_ARG, "sp_pad_mask: mask_out is NULL");
     cudaStream_t st = (cudaStream_t)stream;
     DeviceInfo di;
     int rc = device_info(&di);

@@ -257,3 +257,40 @@ def test_captured_step_replays_the_eager_step_bitwise(name, kw):
     assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
     assert sp.sp_workspace_status(step.ws_attn)[0] == 0
+
+
+@pytest.mark.parametrize("B,T,kw", [(1, 0, {}), (0, 37, {}), (2, 0, dict(fused=True)), (1, 0, dict(Tq=5)),
+                                     (1, 0, dict(direct=True)), (0, 256, dict(direct=True, fused=True)),
+                                     (1, 1, {})])
+def test_degenerate_sizes(B, T, kw):
+    # Empty batches, empty sequences and a single token pass through every
+    # stage without a launch error; a single token equals its own value row.
+    W, H, D = 2, 4, 64
+    step = sp.SPStep(W, B, T, H, D, dtype=torch.bfloat16, **kw)
+    g = torch.Generator().manual_seed(T + B)
+    q = torch.randn(B, kw.get("Tq", T), H, D, generator=g).bfloat16().cuda()
+    k = torch.randn(B, T, H, D, generator=g).bfloat16().cuda()
+    v = torch.randn(B, T, H, D, generator=g).bfloat16().cuda()
+    out = step(q, k, v)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (B, kw.get("Tq", T), H, D)
+    assert sp.sp_workspace_status(step.ws_exchange)[0] == 0
+    if B and T == 1 and "Tq" not in kw:
+        assert torch.equal(out.view(torch.int16), v.view(torch.int16))  # softmax over one key is exactly 1
+    if B and T == 0 and "Tq" in kw:
+        assert (out.float() == 0).all()  # no keys: rows are 0
+
+
+def test_empty_layout_calls():
+    W, H, D = 4, 8, 16
+    ws = sp.new_workspace()
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
+    sp.sp_pad(e(0, 5, H, D), e(0, 8, H, D))
+    sp.sp_tile(e(1, 0, H, D), [e(1, 0, H, D) for _ in range(W)])
+    sp.sp_send_recv_heads([e(1, 0, H, D) for _ in range(W)], [e(1, 0, H // W, D) for _ in range(W)], ws)
+    sp.sp_gather_heads([e(1, 0, H // W, D) for _ in range(W)], [e(1, 0, H, D) for _ in range(W)], ws)
+    sp.sp_pad_send_heads(e(1, 0, H, D), [e(1, 0, H // W, D) for _ in range(W)], ws)
+    sp.sp_gather_output([e(2, 0, H, D) for _ in range(W)], e(2, 0, H, D))
+    sp.sp_unpad(e(0, 4, H, D), e(0, 3, H, D))
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
