@@ -423,3 +423,22 @@ def test_sp_step_2d_equals_unsharded_attention():
     got = oracle.sp_step_2d(q, k, v, grid, W)
     want = oracle.attention(q, k, v)
     assert np.abs(got - want).max() < 1e-12
+
+
+@pytest.mark.parametrize("W", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", list(range(1, 9)))
+def test_sp_step_exhaustive_tiny(W, T):
+    # Every tiny case: T <= 8 tokens on W in {1, 2, 4, 8} ranks (pure-pad
+    # ranks included when T < W), key-only and user masks.  The composition
+    # pad -> tile -> exchange -> attention -> gather -> unpad is plain
+    # attention exactly: same fp64 sums, the pad keys contribute nothing.
+    rng = _rng(100 * W + T)
+    B, H, D = 2, 8, 3
+    q, k, v = (rng.standard_normal((B, T, H, D)).astype(np.float32) for _ in range(3))
+    got = oracle.sp_step(q, k, v, W)
+    assert got.shape == (B, T, H, D) and np.isfinite(got).all()
+    assert np.array_equal(got, oracle.attention(q, k, v))
+    user = (rng.random((B, T, T)) < 0.5).astype(np.uint8)
+    user[:, np.arange(T), np.arange(T)] = 1
+    got = oracle.sp_step(q, k, v, W, user_mask=user)
+    assert np.array_equal(got, oracle.attention(q, k, v, oracle.MASK_FULL, user))
