@@ -2,6 +2,7 @@
 // sp_attention entry point (argument validation and kernel selection).
 #include <math.h>
 #include <atomic>
+#include <mutex>
 #include <stdarg.h>
 #include <string.h>
 
@@ -23,11 +24,13 @@ int set_error(int code, const char *fmt, ...) {
 }
 
 int device_info(DeviceInfo *out) {
+    // per-device cache, published with release / read with acquire (callers
+    // may be on several host threads; a racing first fill writes equal values)
     static DeviceInfo cache[64];
-    static bool have[64] = {false};
+    static std::atomic<bool> have[64];
     int dev = 0;
     SP_CUDA_CHECK(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && have[dev]) {
+    if (dev >= 0 && dev < 64 && have[dev].load(std::memory_order_acquire)) {
         *out = cache[dev];
         return SP_OK;
     }
@@ -41,9 +44,13 @@ int device_info(DeviceInfo *out) {
     SP_CUDA_CHECK(cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
     d.l2_bytes = (size_t)l2;
     d.max_smem_optin = (size_t)smem;
-    if (dev >= 0 && dev < 64) {
-        cache[dev] = d;
-        have[dev] = true;
+    if (dev >= 0 && dev < 64 && !have[dev].load(std::memory_order_acquire)) {
+        static std::mutex fill;
+        std::lock_guard<std::mutex> lock(fill);
+        if (!have[dev].load(std::memory_order_relaxed)) {
+            cache[dev] = d;
+            have[dev].store(true, std::memory_order_release);
+        }
     }
     *out = d;
     return SP_OK;

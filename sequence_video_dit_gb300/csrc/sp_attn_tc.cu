@@ -31,6 +31,7 @@
 // Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
 // SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
 // (again with a bound) and TMEM is freed before the CTA exits.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -1112,13 +1113,16 @@ bool attn_tc_supported(const AttnArgs &a) {
 
 template <int D, bool SPLIT, int MODE>
 static int launch_tc_t(const tc::TcParams &prm, unsigned grid, cudaStream_t st) {
-    static int configured_dev = -1;
+    // the shared-memory opt-in is a per-device attribute of each instance: set
+    // once per device (a bit per device; a racing second set is harmless)
+    static std::atomic<uint64_t> configured{0};
     int dev = 0;
-    cudaGetDevice(&dev);
+    SP_CUDA_CHECK(cudaGetDevice(&dev));
     auto kern = tc::attn_tc_kernel<D, SPLIT, MODE>;
-    if (configured_dev != dev) {
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         SP_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<D>::SMEM_ALLOC));
-        configured_dev = dev;
+        configured.fetch_or(bit, std::memory_order_release);
     }
     if (MODE == 0) {
         kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);

@@ -278,3 +278,44 @@ def test_attention_from_shards_refuses_what_it_cannot_do():
     with pytest.raises(ValueError):  # no tensor-core kernel for fp32
         x = mk(128, torch.float32)
         sp.sp_attention_shards(x, x, x, mk(128, torch.float32), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV)
+
+
+def test_concurrent_host_threads_give_the_same_bytes():
+    # ctypes drops the GIL around each call, so four host threads really enter
+    # the library together (first-use caches included: a fresh process
+    # would fill them here), each on its own stream and workspace.
+    import threading
+
+    W, B, T, Hl, D = 2, 1, 700, 2, 128
+    g = torch.Generator().manual_seed(31)
+    q, k, v = (_mk(W, B, T, Hl, D, torch.bfloat16, g) for _ in range(3))
+    need = sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16)
+    ref = [torch.empty_like(x) for x in q]
+    sp.sp_attention(q, k, v, ref, sp.new_workspace(need))
+    torch.cuda.synchronize()
+    outs, errors = [], []
+
+    def work():
+        try:
+            s = torch.cuda.Stream()
+            ws = sp.new_workspace(need)
+            o = [torch.empty_like(x) for x in q]
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    sp.sp_attention(q, k, v, o, ws, stream=s)
+            s.synchronize()
+            outs.append((o, sp.sp_workspace_status(ws, stream=s)[0]))
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work) for _ in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert len(outs) == 4
+    for o, st in outs:
+        assert st == 0
+        for a, b in zip(o, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
