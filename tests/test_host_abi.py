@@ -108,3 +108,25 @@ def test_header_constants_match_the_binding():
     for name in ("SP_WORKSPACE_HEADER_BYTES", "SP_WORKSPACE_KV_STALL_OFFSET"):
         m = re.search(rf"#define\s+{name}\s+(\d+)", src)
         assert m and int(m.group(1)) == getattr(_lib, name)
+
+
+def test_missing_library_fails_loudly():
+    # No CPU fallback: without the built CUDA library every entry point raises.
+    import subprocess
+    import sys
+
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import sequence_video_dit_gb300._lib as L\n"
+        "L.LIB_PATH = '/nonexistent/libsp_gb300.so'\n"
+        "import sequence_video_dit_gb300 as sp\n"
+        "try:\n"
+        "    sp.sp_padded_len(37, 2)\n"
+        "except ImportError as e:\n"
+        "    print('raised:', e)\n"
+        "    sys.exit(0)\n"
+        "sys.exit(3)\n" % ROOT
+    )
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert p.returncode == 0, p.stdout + p.stderr
+    assert "raised" in p.stdout
