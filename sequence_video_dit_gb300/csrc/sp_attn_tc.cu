@@ -28,6 +28,16 @@
 // a tile's max exceeds it by more than 8 (log2 units), which keeps every
 // probability <= 2^8 and makes O rescales rare.
 //
+// Work decomposition (plan_split): a work item is one (rank, batch, head,
+// query pair).  Short query sequences (fewer items than SMs) cut every item
+// into key pieces, and a last, partial wave of items is cut likewise; the
+// pieces' fp32 partials are merged by LSE in attn_merge_kernel.
+// Operands are either each rank's tensors or, for the exchange fused into
+// the attention, the source ranks' token shards (tile_source picks the shard
+// a 128-row tile lives in).  Three CTA layouts share this code: MODE 0 (the
+// default), MODE 1 (2-CTA clusters multicasting K/V halves) and MODE 2
+// (cta_group::2, M = 256 over a CTA pair); all give the same bits.
+//
 // Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
 // SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
 // (again with a bound) and TMEM is freed before the CTA exits.
