@@ -34,9 +34,7 @@
 // pieces' fp32 partials are merged by LSE in attn_merge_kernel.
 // Operands are either each rank's tensors or, for the exchange fused into
 // the attention, the source ranks' token shards (tile_source picks the shard
-// a 128-row tile lives in).  Three CTA layouts share this code: MODE 0 (the
-// default), MODE 1 (2-CTA clusters multicasting K/V halves) and MODE 2
-// (cta_group::2, M = 256 over a CTA pair); all give the same bits.
+// a 128-row tile lives in).
 //
 // Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
 // SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
@@ -46,7 +44,6 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include "sp_attn.cuh"
@@ -71,9 +68,8 @@ struct Cfg {
 
 struct alignas(128) TcParams {
     CUtensorMap tq[SP_MAX_RANKS], tk[SP_MAX_RANKS], tv[SP_MAX_RANKS], to[SP_MAX_RANKS];
-    CUtensorMap tk_half[SP_MAX_RANKS];  // 64-key box, for the CTA-pair mode
     int W, B, Tq, Tk, Hl;
-    int n_qpairs, n_qp_grid, n_kv, n_split, kv_per_split;
+    int n_qpairs, n_kv, n_split, kv_per_split;
     int n_full;  // SPLIT launches: work items [0, n_full) run whole, the rest in n_split key pieces
     // > 0: Q/O (resp. K/V) maps are per source token shard of this many rows,
     // addressed with head r * Hl + h; a 128-row tile never straddles shards
@@ -142,51 +138,6 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, vol
     if (mbar_try_wait(smem_u32(bar), parity)) return true;
     return wait_slow(bar, parity, abort_flag, status);
 }
-// Cluster-scope acquire: for barriers that the partner CTA arrives on remotely.
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-__device__ __noinline__ bool wait_slow_cl(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = globaltimer();
-    while (true) {
-        for (int i = 0; i < 32; i++)
-            if (mbar_try_wait_cl(a, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            atomicCAS(status, 0, SP_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-__device__ __forceinline__ bool wait_bounded_cl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                                int *status) {
-    if (mbar_try_wait_cl(smem_u32(bar), parity)) return true;
-    return wait_slow_cl(bar, parity, abort_flag, status);
-}
-// Address of the same shared-memory object in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa_rank(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Relaxed remote arrival: for signals whose payload is ordered by tcgen05
-// fences (TMEM contents), not by the generic memory model.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
 // Drain wait (teardown after an abort): bounded, ignores the abort flag.
 __device__ __noinline__ void wait_drain(uint64_t *bar, uint32_t parity) {
     const uint32_t a = smem_u32(bar);
@@ -205,34 +156,6 @@ __device__ __forceinline__ void tma_load_4d(uint64_t *bar, const CUtensorMap *m,
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
         : "memory");
-}
-// Same copy, delivered to the same shared-memory offset of every CTA in
-// `mask` (this cluster), each of whose barriers at `bar`'s offset gets the bytes.
-__device__ __forceinline__ void tma_load_4d_mc(uint64_t *bar, const CUtensorMap *m, uint32_t dst, int c0, int c1,
-                                               int c2, int c3, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-// CTA-pair load: lands in this CTA's shared memory, completes the barrier at
-// `bar_cluster` (a shared::cluster address, here the pair leader's barrier).
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t bar_cluster, const CUtensorMap *m, uint32_t dst, int c0,
-                                                 int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster)
-        : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2,
                                              int c3) {
@@ -280,39 +203,6 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// CTA-pair forms: one thread of the leader CTA issues for both CTAs; A and D
-// rows are split between the CTAs (128 each), B is split along N.
-__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void mma2_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma2_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
 // D(tmem) (+)= A(smem) * B(smem)
 __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -327,14 +217,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
         "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// Commit whose arrival lands on the barrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -486,23 +368,11 @@ __device__ __forceinline__ void tile_source(int shard_rows, int row, int r, int 
 }
 
 // ------------------------------------------------------------------ kernel
-// MC: the grid is made of 2-CTA clusters whose CTAs serve adjacent query pairs
-// of the same (rank, batch, head); each CTA loads one 64-column half of every
-// K/V tile and multicasts it to both, so a K/V tile leaves L2 once per four
-// query tiles instead of once per two.
-//
-// MODE 2 (PAIR): the same 2-CTA clusters, but the tensor core of the pair works
-// as one: the leader CTA's MMA thread issues tcgen05.mma.cta_group::2 with
-// M = 256 (128 query rows in each CTA's TMEM), so each CTA stages only half of
-// every K tile (64 keys) and half of every V tile (64 columns).  The partner
-// relays "my half has landed" and "my P is ready" to the leader's barriers.
-template <int D, bool SPLIT, int MODE>
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
-    constexpr bool MC = MODE == 1;
-    constexpr bool PAIR = MODE == 2;
-    constexpr int NSLOT = PAIR ? 2 * C::NSLOT : C::NSLOT;  // ring slots
-    constexpr int SLOT = PAIR ? C::TILE / 2 : C::TILE;     // bytes per slot
+    constexpr int NSLOT = C::NSLOT;  // ring slots
+    constexpr int SLOT = C::TILE;    // bytes per slot
     extern __shared__ uint8_t dsm_raw[];
     __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_empty[NSLOT];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
@@ -515,8 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     uint8_t *const sgen = dsm_raw + (sbase - raw);
 
     // work item: blockIdx.x -> (rank, batch, head, key split, query pair), query pair
-    // fastest; with MC, n_qp_grid rounds n_qpairs up to even and a surplus CTA
-    // (qp == n_qpairs) only helps load K/V for its cluster partner
+    // fastest
     //
     // SPLIT launches: CTAs [0, n_full) take work items [0, n_full) whole; each
     // later item (the ones that would otherwise form a last, partial wave, or
@@ -527,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     int64_t witem = 0;  // work item, (((r * B + b) * Hl + h) * n_qpairs + qp)
     int kv0, kv1;
     if (!SPLIT) {
-        qp = bid % p.n_qp_grid;
-        bid /= p.n_qp_grid;
+        qp = bid % p.n_qpairs;
+        bid /= p.n_qpairs;
         // (n_split is 1 here; the key range is still derived from the grid,
         // which keeps this instance's code as it measured fastest)
         const int split = bid % p.n_split;
@@ -556,20 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // CTAs of one head run in step; starting each query pair at a different key
     // tile spreads their concurrent K/V reads over L2 instead of all CTAs asking
     // for the same tile at once.  Softmax is order-free, so only rounding moves.
-    const int rot = nkv > 0 ? (int)(((unsigned)(qp >> 1) * 7u) % (unsigned)nkv) : 0;  // same in both CTAs of a cluster
-    const uint32_t crank = (MC || PAIR) ? cluster_ctarank() : 0u;
-    const bool leader = crank == 0;
+    const int rot = nkv > 0 ? (int)(((unsigned)(qp >> 1) * 7u) % (unsigned)nkv) : 0;
     auto key_tile = [&](int jj) { int t = jj + rot; return kv0 + (t >= nkv ? t - nkv : t); };
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
         for (int s = 0; s < NSLOT; s++) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], MC ? 2 : 1);  // with MC both CTAs must release a slot
+            mbar_init(&bar_empty[s], 1);
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar_sf[i], 1);
-            mbar_init(&bar_pf[i], (PAIR && leader) ? 132 : 128);  // + one relay per partner warp
+            mbar_init(&bar_pf[i], 128);
             mbar_init(&bar_of[i], 1);
         }
         mbar_init(&bar_drain, 1);
@@ -577,17 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         fence_mbarrier_init();
     }
     if (warp == 9) {
-        if (PAIR) {  // one warp of each CTA of the pair allocates the pair's TMEM together
-            tmem_alloc2(smem_u32(&tmem_base_sh), 512);
-            tmem_relinquish2();
-        } else {
-            tmem_alloc(smem_u32(&tmem_base_sh), 512);
-            tmem_relinquish();
-        }
+        tmem_alloc(smem_u32(&tmem_base_sh), 512);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
-    if (MC || PAIR) cluster_sync();  // the partner's barriers exist before anything reaches them
     tc_fence_after();
     const uint32_t tbase = tmem_base_sh;
     volatile int *abort_flag = &abort_sh;
@@ -598,17 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             prefetch_tmap(&p.tq[r]);
             prefetch_tmap(&p.tk[r]);
             prefetch_tmap(&p.tv[r]);
-            // pair mode: every load of both CTAs completes the leader's barrier, which
-            // the leader arms for both CTAs' bytes; the partner never arms it
-            const uint32_t lq = PAIR ? mapa_rank(smem_u32(&bar_q), 0) : 0u;
-            if (!PAIR || leader) mbar_arrive_expect_tx(&bar_q, (PAIR ? 4 : 2) * C::TILE);
+            mbar_arrive_expect_tx(&bar_q, 2 * C::TILE);
             for (int i = 0; i < 2; i++) {
                 int qmap, qhead, qrow;
                 tile_source(p.q_shard_rows, qp * 256 + i * 128, r, h, p.Hl, p.W, qmap, qhead, qrow);
                 for (int db = 0; db < C::DB; db++) {
                     const uint32_t dst = sbase + C::Q_OFF + i * C::TILE + db * 16384;
-                    if (PAIR) tma_load_4d_pair(lq, &p.tq[r], dst, db * 64, h, qp * 256 + i * 128, b);
-                    else tma_load_4d(&bar_q, &p.tq[qmap], dst, db * 64, qhead, qrow, b);
+                    tma_load_4d(&bar_q, &p.tq[qmap], dst, db * 64, qhead, qrow, b);
                 }
             }
             // load n: K of key tile n/2 (n even) or V (n odd) into slot n % NSLOT
@@ -618,52 +475,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (; n < nloads; n++) {
                 const int slot = n % NSLOT;
                 const int use = n / NSLOT;
-                if (use > 0 && !(PAIR ? wait_bounded_cl(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status)
-                                      : wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status)))
+                if (use > 0 && !wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status))
                     break;
-                if (!PAIR || leader) mbar_arrive_expect_tx(&bar_full[slot], PAIR ? 2 * SLOT : SLOT);
+                mbar_arrive_expect_tx(&bar_full[slot], SLOT);
                 int kmap, khead, kshrow;
                 tile_source(p.kv_shard_rows, key_tile(n >> 1) * 128, r, h, p.Hl, p.W, kmap, khead, kshrow);
                 const CUtensorMap *m = (n & 1) ? &p.tv[kmap] : &p.tk[kmap];
-                const int krow = key_tile(n >> 1) * 128;
-                if (PAIR) {
-                    const uint32_t dst = sbase + C::R_OFF + slot * SLOT;
-                    const uint32_t lb = mapa_rank(smem_u32(&bar_full[slot]), 0);
-                    if (n & 1) {  // V: all 128 keys, this CTA's 64 columns
-                        tma_load_4d_pair(lb, &p.tv[r], dst, (int)crank * 64, h, krow, b);
-                    } else {      // K: this CTA's 64 keys, all columns
-                        for (int db = 0; db < C::DB; db++)
-                            tma_load_4d_pair(lb, &p.tk_half[r], dst + db * 8192, db * 64, h, krow + (int)crank * 64, b);
-                    }
-                } else if (MC) {
-                    // this CTA's half (64 columns) of the tile, written into both CTAs
-                    tma_load_4d_mc(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + crank * 16384, crank * 64, h,
-                                   krow, b, (uint16_t)0x3);
-                } else {
-                    for (int db = 0; db < C::DB; db++)
-                        tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, khead,
-                                    kshrow, b);
-                }
+                for (int db = 0; db < C::DB; db++)
+                    tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, khead,
+                                kshrow, b);
             }
-            if (!PAIR || leader) {
-                // Before the CTA may exit, every load it issued has landed: wait
-                // for the newest load of every slot (older ones were consumed
-                // before their slot was reused).  In a normal run the MMA thread
-                // waits for the same phases; after an abort these bounded waits
-                // keep the teardown from freeing shared memory under a copy.
-                wait_drain(&bar_q, 0);
-                for (int slot = 0; slot < NSLOT && slot < n; slot++) {
-                    const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
-                    wait_drain(&bar_full[slot], (uint32_t)(last / NSLOT) & 1u);
-                }
+            // Before the CTA may exit, every load it issued has landed: wait
+            // for the newest load of every slot (older ones were consumed
+            // before their slot was reused).  In a normal run the MMA thread
+            // waits for the same phases; after an abort these bounded waits
+            // keep the teardown from freeing shared memory under a copy.
+            wait_drain(&bar_q, 0);
+            for (int slot = 0; slot < NSLOT && slot < n; slot++) {
+                const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
+                wait_drain(&bar_full[slot], (uint32_t)(last / NSLOT) & 1u);
             }
         }
         __syncwarp();
     } else if (warp == 9) {
         // ---------------------------------------------------------- MMA issuer
-        // (pair mode: the leader CTA's thread issues for both CTAs)
-        if (lane == 0 && nkv > 0 && (!PAIR || leader)) {
-            constexpr int M = PAIR ? 256 : 128;
+        if (lane == 0 && nkv > 0) {
+            constexpr int M = 128;
             constexpr uint32_t idesc_qk = make_idesc(M, 128, false);
             constexpr uint32_t idesc_pv = make_idesc(M, D, true);
             int issued = 0;
@@ -673,12 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             const uint64_t dq0 = make_sdesc(sbase + C::Q_OFF, 16, 1024);
             const uint64_t dq1 = make_sdesc(sbase + C::Q_OFF + C::TILE, 16, 1024);
             const uint64_t dk0 = make_sdesc(sbase + C::R_OFF, 16, 1024);  // K tile: K-major
-            // V tile: MN-major (d contiguous), 8-key groups 1024 bytes apart; a full
-            // tile's two 64-column blocks are 16 KB apart, a pair half has one block
-            const uint64_t dv0 = make_sdesc(sbase + C::R_OFF, PAIR ? 1024 : 16384, 1024);
+            // V tile: MN-major (d contiguous), 8-key groups 1024 bytes apart, the
+            // tile's two 64-column blocks 16 KB apart
+            const uint64_t dv0 = make_sdesc(sbase + C::R_OFF, 16384, 1024);
             constexpr uint32_t kSlotStep = SLOT >> 4;
-            // K-major column blocks: 16 KB apart in a full K tile, 8 KB in a 64-key half
-            constexpr int kBlk = PAIR ? 512 : 1024;
+            // K-major column blocks: 16 KB apart
+            constexpr int kBlk = 1024;
             auto qk = [&](int i, int slot) {
                 const uint64_t a = i ? dq1 : dq0;
                 const uint64_t bk = dk0 + (uint64_t)(slot * kSlotStep);
@@ -687,8 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 for (int kk = 0; kk < D / 16; kk++) {
                     const uint64_t oa = (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2);  // Q: (kk/4)*16 KB + (kk%4)*32 B
                     const uint64_t ob = (uint64_t)((kk >> 2) * kBlk + (kk & 3) * 2);
-                    if (PAIR) mma2_ss(d, a + oa, bk + ob, idesc_qk, kk > 0 ? 1u : 0u);
-                    else mma_ss(d, a + oa, bk + ob, idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_ss(d, a + oa, bk + ob, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 issued = 1;
             };
@@ -698,40 +534,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const uint32_t pa = tbase + (uint32_t)(i * 128);
 #pragma unroll
                 for (int kk = 0; kk < 8; kk++) {  // 16 keys (2048 bytes of V) per step, all D columns at once
-                    if (PAIR)
-                        mma2_ts(d, pa + (uint32_t)(kk * 8), bv + (uint64_t)(kk * 128), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-                    else
-                        mma_ts(d, pa + (uint32_t)(kk * 8), bv + (uint64_t)(kk * 128), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+                    mma_ts(d, pa + (uint32_t)(kk * 8), bv + (uint64_t)(kk * 128), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
                 }
                 issued = 1;
             };
-            // barrier signals go to every CTA whose TMEM or shared memory the MMAs used
-            auto signal = [&](uint64_t *bar) {
-                if (PAIR) mma2_commit_mc(bar, (uint16_t)0x3);
-                else mma_commit(bar);
-            };
+            auto signal = [&](uint64_t *bar) { mma_commit(bar); };
             // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
             auto kslot = [](int j) { return (2 * j) % NSLOT; };
-            // a slot is free once every CTA that received the tile has consumed it
-            auto release = [&](int slot) {
-                if (PAIR) mma2_commit_mc(&bar_empty[slot], (uint16_t)0x3);
-                else if (MC) mma_commit_mc(&bar_empty[slot], (uint16_t)0x3);
-                else mma_commit(&bar_empty[slot]);
-            };
+            // a slot is free once the MMAs that read it have completed
+            auto release = [&](int slot) { mma_commit(&bar_empty[slot]); };
             auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };
             auto kpar = [](int j) { return (uint32_t)((2 * j) / NSLOT) & 1u; };
             auto vpar = [](int j) { return (uint32_t)((2 * j + 1) / NSLOT) & 1u; };
-            // a ring slot is ready when its barrier saw every byte (pair mode: both CTAs' halves)
+            // a ring slot is ready when its barrier saw every byte
             auto slot_ready = [&](int slot, uint32_t par) {
-                return PAIR ? wait_bounded_cl(&bar_full[slot], par, abort_flag, p.status)
-                            : wait_bounded(&bar_full[slot], par, abort_flag, p.status);
+                return wait_bounded(&bar_full[slot], par, abort_flag, p.status);
             };
-            auto p_ready = [&](int i, uint32_t par) {
-                return PAIR ? wait_bounded_cl(&bar_pf[i], par, abort_flag, p.status)
-                            : wait_bounded(&bar_pf[i], par, abort_flag, p.status);
-            };
-            bool ok = (PAIR ? wait_bounded_cl(&bar_q, 0, abort_flag, p.status) : wait_bounded(&bar_q, 0, abort_flag, p.status)) &&
-                      slot_ready(kslot(0), kpar(0));
+            auto p_ready = [&](int i, uint32_t par) { return wait_bounded(&bar_pf[i], par, abort_flag, p.status); };
+            bool ok = wait_bounded(&bar_q, 0, abort_flag, p.status) && slot_ready(kslot(0), kpar(0));
             if (ok) {
                 tc_fence_after();
                 qk(0, kslot(0));
@@ -767,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 }
             }
             if (*abort_flag && issued) {
-                if (PAIR) mma2_commit_mc(&bar_drain, (uint16_t)0x1);
-                else mma_commit(&bar_drain);
+                mma_commit(&bar_drain);
                 wait_drain(&bar_drain, 0);
             }
         }
@@ -790,8 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (nkv > 0) mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
         for (int jj = 0; jj < nkv; jj++) {
-            const bool s_ok = PAIR ? wait_bounded_cl(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status)
-                                   : wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status);
+            const bool s_ok = wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status);
             if (!__all_sync(0xffffffffu, s_ok)) {  // leave together: the loop body is warp-collective
                 ok = false;
                 break;
@@ -857,14 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             tmem_st_wait();
             tc_fence_before();
-            if (PAIR && !leader) {
-                // P lives in this CTA's TMEM but the leader issues the MMA: each
-                // warp relays one arrival once its 32 rows are stored
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote_relaxed(mapa_rank(smem_u32(&bar_pf[i]), 0));
-            } else {
-                mbar_arrive(&bar_pf[i]);
-            }
+            mbar_arrive(&bar_pf[i]);
             if (jj + 1 < nkv) mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
         }
         // the epilogue has a 128-thread barrier: the tile's four warps decide together
@@ -872,8 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (epi && qp < p.n_qpairs) {
             bool have = true;
             if (nkv > 0) {
-                have = PAIR ? wait_bounded_cl(&bar_of[i], 0, abort_flag, p.status)
-                            : wait_bounded(&bar_of[i], 0, abort_flag, p.status);
+                have = wait_bounded(&bar_of[i], 0, abort_flag, p.status);
                 // the four warps decide together: the store below has a
                 // 128-thread barrier that no warp may reach alone
                 have = named_bar_and(1 + i, 128, have);
@@ -943,15 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();  // the pair's TMEM is freed by both CTAs together, after both are done
     tc_fence_after();
-    if (warp == 9) {
-        if (PAIR) tmem_dealloc2(tbase, 512);
-        else tmem_dealloc(tbase, 512);
-    }
-    // the partner may still be delivering into this CTA's shared memory or
-    // barriers until it is done too
-    if (MC || PAIR) cluster_sync();
+    if (warp == 9) tmem_dealloc(tbase, 512);
 }
 
 // Merge of split-key partials: one warp per (rank, batch, head, query) row.
@@ -1022,14 +825,13 @@ static int get_encode() {
     return SP_OK;
 }
 
-// 4-D map over (d, head, token, batch) with a 64 x 1 x box_rows x 1 box, 128-byte swizzle.
-static int encode_map(CUtensorMap *m, const void *base, int D, int Hl, int T, int B, const int64_t st[3],
-                      int box_rows = 128) {
+// 4-D map over (d, head, token, batch) with a 64 x 1 x 128 x 1 box, 128-byte swizzle.
+static int encode_map(CUtensorMap *m, const void *base, int D, int Hl, int T, int B, const int64_t st[3]) {
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hl, (cuuint64_t)T, (cuuint64_t)B};
     // strides of a size-1 dim do not matter; give them a legal value
     int64_t hs = Hl > 1 ? st[2] : D, ts = T > 1 ? st[1] : (int64_t)Hl * hs, bs = B > 1 ? st[0] : (int64_t)T * ts;
     cuuint64_t strides[3] = {(cuuint64_t)hs * 2, (cuuint64_t)ts * 2, (cuuint64_t)bs * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t box[4] = {64, 1, 128, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult rc = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1121,40 +923,21 @@ bool attn_tc_supported(const AttnArgs &a) {
     return true;
 }
 
-template <int D, bool SPLIT, int MODE>
+template <int D, bool SPLIT>
 static int launch_tc_t(const tc::TcParams &prm, unsigned grid, cudaStream_t st) {
     // the shared-memory opt-in is a per-device attribute of each instance: set
     // once per device (a bit per device; a racing second set is harmless)
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     SP_CUDA_CHECK(cudaGetDevice(&dev));
-    auto kern = tc::attn_tc_kernel<D, SPLIT, MODE>;
+    auto kern = tc::attn_tc_kernel<D, SPLIT>;
     const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
     if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         SP_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<D>::SMEM_ALLOC));
         configured.fetch_or(bit, std::memory_order_release);
     }
-    if (MODE == 0) {
-        kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);
-        return check_launch("sp_attention(tcgen05)");
-    }
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(tc::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = tc::Cfg<D>::SMEM_ALLOC;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, prm);
-    if (e != cudaSuccess)
-        return set_error(SP_ERR_CUDA, "sp_attention(tcgen05, cluster) launch failed: %s", cudaGetErrorString(e));
-    return check_launch("sp_attention(tcgen05, cluster)");
+    kern<<<grid, tc::kThreads, tc::Cfg<D>::SMEM_ALLOC, st>>>(prm);
+    return check_launch("sp_attention(tcgen05)");
 }
 
 int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
@@ -1172,7 +955,6 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     for (int r = 0; r < a.W; r++) {
         if ((rc = tc::encode_map(&prm.tq[r], a.q[r], a.D, qh, qt, a.B, a.qs))) return rc;
         if ((rc = tc::encode_map(&prm.tk[r], a.k[r], a.D, kh, kt, a.B, a.ks))) return rc;
-        if ((rc = tc::encode_map(&prm.tk_half[r], a.k[r], a.D, kh, kt, a.B, a.ks, 64))) return rc;
         if ((rc = tc::encode_map(&prm.tv[r], a.v[r], a.D, kh, kt, a.B, a.ks))) return rc;
         if ((rc = tc::encode_map(&prm.to[r], a.o[r], a.D, qh, qt, a.B, a.os))) return rc;
     }
@@ -1191,20 +973,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.Tq = a.Tq;
     prm.Tk = a.Tk;
     prm.Hl = a.Hl;
-    // With several query pairs per head, CTA pairs may share each K/V tile:
-    // MODE 2 (one M=256 tensor-core pass per pair) or MODE 1 (multicast loads,
-    // separate M=128 passes).  Both measure the same as MODE 0 (independent
-    // CTAs), which stays the default; SP_ATTN_CLUSTER_MODE=0/1/2 selects one.
-    static const int mode_env = [] {
-        const char *e = getenv("SP_ATTN_CLUSTER_MODE");
-        return (e && e[0] >= '0' && e[0] <= '2' && e[1] == 0) ? e[0] - '0' : -1;
-    }();
-    const bool pairable = a.D == 128 && sp.n_split == 1 && sp.n_qpairs >= 2 && a.q_shard_rows == 0 &&
-                          a.kv_shard_rows == 0;
-    const int mode = pairable ? (mode_env >= 0 ? mode_env : 0) : 0;
-    const bool mc = mode != 0;
     prm.n_qpairs = sp.n_qpairs;
-    prm.n_qp_grid = mc ? (sp.n_qpairs + 1) & ~1 : sp.n_qpairs;
     prm.n_kv = sp.n_kv;
     prm.n_split = sp.n_split;
     prm.kv_per_split = sp.kv_per_split;
@@ -1216,14 +985,14 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.status = &a.ws->status;
     prm.kv_stall = &a.ws->kv_stall;
     const int64_t grid = sp.n_split > 1 ? (int64_t)sp.n_full + (int64_t)sp.n_pieced * sp.n_split
-                                        : (int64_t)a.W * a.B * a.Hl * prm.n_qp_grid;
+                                        : (int64_t)a.W * a.B * a.Hl * sp.n_qpairs;
     if (grid == 0) return SP_OK;
     if (grid > 0x7fffffffll) return set_error(SP_ERR_INVALID_ARG, "sp_attention: grid too large");
     if (sp.n_split > 1) {
         prm.part_o = reinterpret_cast<float *>(a.extra);
         prm.part_lse = prm.part_o + (size_t)sp.n_pieced * sp.n_split * 256 * a.D;
-        rc = (a.D == 64) ? launch_tc_t<64, true, 0>(prm, (unsigned)grid, st)
-                         : launch_tc_t<128, true, 0>(prm, (unsigned)grid, st);
+        rc = (a.D == 64) ? launch_tc_t<64, true>(prm, (unsigned)grid, st)
+                         : launch_tc_t<128, true>(prm, (unsigned)grid, st);
         if (rc) return rc;
         tc::MergeParams mp;
         memset(&mp, 0, sizeof(mp));
@@ -1247,10 +1016,8 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);
         return check_launch("sp_attention(merge)");
     }
-    if (a.D == 64) return launch_tc_t<64, false, 0>(prm, (unsigned)grid, st);
-    if (mode == 2) return launch_tc_t<128, false, 2>(prm, (unsigned)grid, st);
-    if (mode == 1) return launch_tc_t<128, false, 1>(prm, (unsigned)grid, st);
-    return launch_tc_t<128, false, 0>(prm, (unsigned)grid, st);
+    if (a.D == 64) return launch_tc_t<64, false>(prm, (unsigned)grid, st);
+    return launch_tc_t<128, false>(prm, (unsigned)grid, st);
 }
 
 }  // namespace sp
