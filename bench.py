@@ -23,6 +23,7 @@ barrier and the max-over-ranks timing reduction are the only collectives.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -156,20 +157,75 @@ def weak_scaling_value(flops_per_rank: float, world: int, seconds_max: float) ->
     return flops_per_rank * world / seconds_max / 1e12
 
 
-def attention_traffic_bytes(name: str):
-    """DRAM bytes (read + write) per attention launch from the committed ncu
-    summary (profiles/attention_dram.md), or None when it has no row."""
-    import re
+# DRAM traffic of the attention kernel comes from one ncu capture, recorded
+# as JSON beside the profiles together with a digest of the kernel's source;
+# a record taken on other source is stale and gives no traffic figure.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_dram.json")
+ATTN_SOURCES = ("sequence_video_dit_gb300/csrc/sp_attn_tc.cu", "sequence_video_dit_gb300/csrc/sp_attn.cuh",
+                "sequence_video_dit_gb300/csrc/sp_internal.cuh")
 
-    path = os.path.join(ROOT, "profiles", "attention_dram.md")
-    if not os.path.exists(path):
-        return None
-    with open(path) as f:
-        for line in f:
-            m = re.match(r"\|\s*(c\d)\s*\|\s*([0-9.]+)\s*\|\s*([0-9.]+)\s*\|", line)
-            if m and m.group(1) == name:
-                return int(round((float(m.group(2)) + float(m.group(3))) * 1e6))
-    return None
+
+def attention_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def attention_traffic(name: str):
+    """(DRAM bytes read + written per attention launch, provenance) for
+    workload `name`, or (None, why not)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu record"
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f).get(name)
+    if not rec:
+        return None, f"no ncu record for {name}"
+    if rec.get("source_digest") != attention_source_digest():
+        return None, "ncu record taken on other attention source (stale)"
+    return int(rec["dram_bytes_per_launch"]), f"ncu, attention source {rec['source_digest']}"
+
+
+_UNIT_SCALE = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+
+
+def record_traffic(csv_path: str, name: str, command: str) -> dict:
+    """Reads an ncu --csv metrics log (dram__bytes_read.sum and
+    dram__bytes_write.sum of attn_tc_kernel launches) and stores the mean
+    per-launch traffic for workload `name` in the JSON record."""
+    import csv
+
+    per_launch = {}
+    with open(csv_path, newline="") as f:
+        rows = [r for r in csv.reader(f) if r]
+    head = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    cols = rows[head]
+    c_id, c_k, c_m, c_u, c_v = (cols.index(n) for n in ("ID", "Kernel Name", "Metric Name", "Metric Unit",
+                                                         "Metric Value"))
+    for r in rows[head + 1:]:
+        if len(r) <= c_v or "attn_tc_kernel" not in r[c_k]:
+            continue
+        if r[c_m] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(r[c_v].replace(",", "")) * _UNIT_SCALE.get(r[c_u].strip().lower(), 1)
+        per_launch.setdefault(r[c_id], {})[r[c_m]] = val
+    full = [d for d in per_launch.values() if len(d) == 2]
+    if not full:
+        raise SystemExit(f"no attn_tc_kernel DRAM counters in {csv_path}")
+    rd = statistics.mean(d["dram__bytes_read.sum"] for d in full)
+    wr = statistics.mean(d["dram__bytes_write.sum"] for d in full)
+    data = {}
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    data[name] = {"kernel": "attn_tc_kernel", "launches": len(full), "dram_read_bytes": int(rd),
+                  "dram_write_bytes": int(wr), "dram_bytes_per_launch": int(rd + wr),
+                  "source_digest": attention_source_digest(), "command": command}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return data[name]
 
 
 def workload_config(wl, world: int, big_inputs: bool) -> dict:
@@ -289,10 +345,14 @@ def run_ours(args, world, rank, local):
     h2d = in_bytes + (um_host.numel() if um_host is not None else 0)
     d2h = out_host.numel() * out_host.element_size()
     e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev)
+    link = measure_link(host, out_host, dev)
+    # lower bound of a pipelined end-to-end step: the slower of the device
+    # step and the step's copies over the link (both directions at once)
+    e2e_bound_ms = max(ms, link["both_directions_ms"])
     peaks = load_peaks()
     achieved = flops / (attn_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
-    traffic = attention_traffic_bytes(wl.name)
+    traffic, traffic_src = attention_traffic(wl.name)
     result = {
         "metric": METRIC,
         "value": round(weak_scaling_value(flops, world, ms_max / 1e3), 3),
@@ -316,11 +376,14 @@ def run_ours(args, world, rank, local):
         "graph_step": graphed,
         "e2e": {"value": round(weak_scaling_value(flops, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "copies": "pinned host buffers; H2D of step i+1 and D2H of step i overlap step i's compute"},
+                "copies": "pinned host buffers on two copy streams; H2D of step i+1 and D2H of step i-1 overlap "
+                          "step i's compute",
+                "link": link, "bound_ms_per_step": round(e2e_bound_ms, 4),
+                "frac_of_bound": round(e2e_bound_ms / e2e_ms, 4)},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_kind": f"bf16 sustained, {peaks['source']}",
+                     "traffic_source": traffic_src, "peak_kind": f"bf16 sustained, {peaks['source']}",
                      "algorithmic_flops_per_launch": flops},
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
@@ -410,9 +473,13 @@ def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> 
 
 def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev) -> float:
     """Mean ms per step of `steps` end-to-end steps (H2D of every step's inputs,
-    the step, D2H of its output), copies overlapped with compute."""
+    the step, D2H of its output).  Uploads and downloads run on two copy
+    streams of their own, so step i+1's uploads, step i's compute and step
+    i-1's download can all be in flight at once (two input and two output
+    buffers, ordered by events)."""
     main = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     d_in = [{n: torch.empty_like(host[n], device=dev) for n in host} for _ in range(2)]
     d_um = [um_host.to(dev) if um_host is not None else None for _ in range(2)]
     d_out = [torch.empty_like(step.out) for _ in range(2)]
@@ -422,40 +489,80 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
     ev_d2h = [torch.cuda.Event() for _ in range(2)]
 
     def upload(slot):
-        for n in host:
-            d_in[slot][n].copy_(host[n], non_blocking=True)
-        if um_host is not None:
-            d_um[slot].copy_(um_host, non_blocking=True)
-        ev_in[slot].record(copy)
+        with torch.cuda.stream(up):
+            for n in host:
+                d_in[slot][n].copy_(host[n], non_blocking=True)
+            if um_host is not None:
+                d_um[slot].copy_(um_host, non_blocking=True)
+            ev_in[slot].record(up)
 
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(main)
-    copy.wait_event(t0)
-    with torch.cuda.stream(copy):
-        upload(0)
+    up.wait_event(t0)
+    down.wait_event(t0)
+    upload(0)
     for i in range(steps):
         b = i % 2
+        if i + 1 < steps:
+            if i >= 1:
+                up.wait_event(ev_done[1 - b])  # step i-1 is done with d_in[1-b]
+            upload(1 - b)
         main.wait_event(ev_in[b])
         if i >= 2:
-            main.wait_event(ev_d2h[b])  # d_out[b] is free again
+            main.wait_event(ev_d2h[b])  # step i-2's output has left d_out[b]
         step(d_in[b]["q"], d_in[b]["k"], d_in[b]["v"], user_mask=d_um[b], out=d_out[b])
         ev_done[b].record(main)
-        with torch.cuda.stream(copy):
-            if i + 1 < steps:
-                if i >= 1:
-                    copy.wait_event(ev_done[1 - b])  # step i-1 is done with d_in[1-b]
-                upload(1 - b)
-            copy.wait_event(ev_done[b])
+        down.wait_event(ev_done[b])
+        with torch.cuda.stream(down):
             out_pin[b].copy_(d_out[b], non_blocking=True)
-            ev_d2h[b].record(copy)
-    main.wait_stream(copy)
+            ev_d2h[b].record(down)
+    main.wait_stream(up)
+    main.wait_stream(down)
     t1.record(main)
     torch.cuda.synchronize()
     barrier(world)
     return max_over_ranks(t0.elapsed_time(t1) / steps, world)
+
+
+def measure_link(host, out_host, dev, reps: int = 3) -> dict:
+    """Host link bandwidth for this step's copies, measured with plain pinned
+    copies of the same tensors: uploads alone, the download alone, and both
+    directions at once on two streams (best of `reps`, CUDA events)."""
+    d_in = {n: torch.empty_like(host[n], device=dev) for n in host}
+    d_out = torch.empty(out_host.shape, dtype=out_host.dtype, device=dev)
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def timed(do_up, do_down):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            main = torch.cuda.current_stream(dev)
+            a.record(main)
+            up.wait_event(a)
+            down.wait_event(a)
+            if do_up:
+                with torch.cuda.stream(up):
+                    for n in host:
+                        d_in[n].copy_(host[n], non_blocking=True)
+            if do_down:
+                with torch.cuda.stream(down):
+                    out_host.copy_(d_out, non_blocking=True)
+            main.wait_stream(up)
+            main.wait_stream(down)
+            z.record(main)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(z))
+        return best
+
+    t_up, t_down, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(h2d / t_up / 1e6, 1), "d2h_gbs": round(d2h / t_down / 1e6, 1),
+            "h2d_ms": round(t_up, 3), "d2h_ms": round(t_down, 3), "both_directions_ms": round(t_both, 3)}
 
 
 # ---------------------------------------------------------------- reference arm (the oracle)
@@ -531,6 +638,27 @@ def run_sweep(args):
         raise RuntimeError(f"exchange status {st}")
 
 
+def run_profile(args):
+    """`--steps` steps of one variant of the step (staged, fused or direct)
+    on the workload's inputs, with no timing and no output: a short program
+    for ncu captures of single kernels."""
+    import sequence_video_dit_gb300 as sp
+
+    wl = workloads.get(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = workloads.make_inputs(wl)
+    d_in = {n: inp[n].to(dev) for n in ("q", "k", "v")}
+    d_um = inp["user_mask"].to(dev) if inp["user_mask"] is not None else None
+    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, device=dev,
+                     fused=args.profile in ("fused", "direct"), direct=args.profile == "direct")
+    for _ in range(args.steps):
+        step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
+    torch.cuda.synchronize()
+    st = sp.sp_workspace_status(step.ws_exchange)[0] | sp.sp_workspace_status(step.ws_attn)[0]
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -539,9 +667,18 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--profile", choices=["staged", "fused", "direct"],
+                    help="run --steps steps of this step variant untimed (a target for ncu) and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the attention kernel's DRAM bytes per launch from an ncu --csv metrics log "
+                         "(taken on --workload) and exit")
+    ap.add_argument("--traffic-command", default="", help="the ncu command that wrote NCU_CSV (stored with it)")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.traffic_command)))
+        return
     if args.warmup < 3 and args.impl == "ours" and not args.sweep:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
@@ -555,6 +692,9 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.profile:
+        run_profile(args)
         return
     res = run_ours(args, world, rank, local)
     if rank == 0:

@@ -243,12 +243,17 @@ SP_API int sp_gather_heads_output(const void *const *heads, void *out, int W, in
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress), so make the first call on each device before
- * any stream capture begins.  Each call clears the counters on `stream`
- * before its kernel runs.  All calls share the one array: calls that overlap
- * on the GPU (other streams, other host threads) race on it; serialise them.
+ * any stream capture begins.  Every argument is checked first: a rejected call
+ * returns its error and leaves the array untouched.  A call that passes the
+ * checks clears the finish ticket and the counters on `stream` before its
+ * kernel runs; the status word is kept.  All calls share the one array: calls
+ * that overlap on the GPU (other streams, other host threads) race on it;
+ * serialise them.
  * status_out (host, may be NULL): when given, the call waits for `stream`,
- * stores the device status of this exchange (SP_OK or SP_ERR_BARRIER) there
- * and resets it; when NULL the call stays asynchronous. */
+ * stores the status word there -- the first device error (SP_ERR_BARRIER)
+ * recorded by any exchange on this device since the last read, else SP_OK --
+ * and resets it to SP_OK; when NULL the call stays asynchronous and an error
+ * it records waits for the next call that reads the status. */
 SP_API int sp_send_recv_heads_noalloc(const void *const *shards, void *const *heads, int W, int B, int Tl,
                                       int H, int D, int elt_bytes, int *status_out, sp_stream_t stream);
 

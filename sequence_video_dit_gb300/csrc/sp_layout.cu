@@ -388,9 +388,9 @@ static int launch_exchange_fused(void *x, void *const *heads, int W, int B, int 
     return check_launch(what);
 }
 
-template <bool GATHER>
-static int launch_exchange(const void *const *src, void *const *dst, int W, int B, int Tl, int H,
-                           int D, int elt, void *workspace, cudaStream_t st, const char *what) {
+// Host-side checks and kernel parameters of one exchange (nothing is issued).
+static int prepare_exchange(const void *const *src, void *const *dst, int W, int B, int Tl, int H, int D, int elt,
+                            void *workspace, const char *what, ExchangeParams &p, int &V) {
     if (W < 1 || W > SP_MAX_RANKS) return set_error(SP_ERR_INVALID_ARG, "%s: W=%d out of [1,%d]", what, W, SP_MAX_RANKS);
     if (B < 0 || Tl < 0 || H < 1 || D < 1) return set_error(SP_ERR_INVALID_ARG, "%s: bad sizes", what);
     if (elt != 1 && elt != 2 && elt != 4 && elt != 8) return set_error(SP_ERR_INVALID_ARG, "%s: elt_bytes=%d", what, elt);
@@ -398,7 +398,6 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
     if (!src || !dst || !workspace) return set_error(SP_ERR_INVALID_ARG, "%s: null pointer array or workspace", what);
     if (((uintptr_t)workspace & 15) != 0) return set_error(SP_ERR_ALIGNMENT, "%s: workspace not 16-byte aligned", what);
     const int Hl = H / W;
-    ExchangeParams p;
     memset(&p, 0, sizeof(p));
     uint64_t align = 0;
     p.chunk_bytes = (int64_t)Hl * D * elt;
@@ -411,7 +410,7 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
         p.dst[i] = (uint8_t *)dst[i];
         align |= (uint64_t)(uintptr_t)src[i] | (uint64_t)(uintptr_t)dst[i];
     }
-    const int V = vector_width(align ? align : 16);
+    V = vector_width(align ? align : 16);
     p.W = W;
     p.Tl = Tl;
     p.T_all = (uint32_t)W * Tl;
@@ -419,7 +418,13 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
     if (chunks > 0x7fffffffull) return set_error(SP_ERR_INVALID_ARG, "%s: too many tokens", what);
     p.chunks_per_rank = (uint32_t)chunks;
     p.ws = (WorkspaceHeader *)workspace;
-    if (chunks == 0) return SP_OK;
+    return SP_OK;
+}
+
+template <bool GATHER>
+static int run_exchange(const ExchangeParams &p, int V, cudaStream_t st, const char *what) {
+    if (p.chunks_per_rank == 0) return SP_OK;
+    const int W = p.W;
     DeviceInfo di;
     int rc = device_info(&di);
     if (rc) return rc;
@@ -435,6 +440,16 @@ static int launch_exchange(const void *const *src, void *const *dst, int W, int 
         default: exchange_kernel<1, GATHER><<<grid, 256, 0, st>>>(p, nvec, tl); break;
     }
     return check_launch(what);
+}
+
+template <bool GATHER>
+static int launch_exchange(const void *const *src, void *const *dst, int W, int B, int Tl, int H,
+                           int D, int elt, void *workspace, cudaStream_t st, const char *what) {
+    ExchangeParams p;
+    int V = 16;
+    int rc = prepare_exchange(src, dst, W, B, Tl, H, D, elt, workspace, what, p, V);
+    if (rc) return rc;
+    return run_exchange<GATHER>(p, V, st, what);
 }
 
 // ---------------------------------------------------------------- allocation-free exchange
@@ -674,10 +689,20 @@ int sp_send_recv_heads_noalloc(const void *const *shards, void *const *heads, in
     int rc = noalloc_scratch(&ws);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    // the counters and the ticket must start at zero; the previous call's
-    // contents are still in the array
-    SP_CUDA_CHECK(cudaMemsetAsync(ws, 0, SP_WORKSPACE_HEADER_BYTES, st));
-    rc = launch_exchange<false>(shards, heads, W, B, Tl, H, D, elt_bytes, ws, st, "sp_send_recv_heads_noalloc");
+    const char *what = "sp_send_recv_heads_noalloc";
+    ExchangeParams p;
+    int V = 16;
+    // every argument is checked before the shared array is touched: a
+    // rejected call leaves it as the previous call left it
+    rc = prepare_exchange(shards, heads, W, B, Tl, H, D, elt_bytes, ws, what, p, V);
+    if (rc) return rc;
+    // the ticket and the counters must start at zero (the previous call's
+    // last CTA reset them; cleared again in case that call never ran to its
+    // end).  The status word is kept: it holds the first device error since
+    // the last read, which a call with status_out reports and resets.
+    SP_CUDA_CHECK(cudaMemsetAsync((uint8_t *)ws + offsetof(WorkspaceHeader, ticket), 0,
+                                  offsetof(WorkspaceHeader, observed) - offsetof(WorkspaceHeader, ticket), st));
+    rc = run_exchange<false>(p, V, st, what);
     if (rc) return rc;
     if (status_out) {
         int s = 0;

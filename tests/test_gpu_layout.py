@@ -141,12 +141,13 @@ def test_argument_errors():
         sp.sp_tile(x, [torch.zeros(1, 18, 4, 8, device="cuda")] * 2)
 
 
-def test_full_size_exchange_round_trip_and_sampled_map():
-    # c5 / sweep scale: 49160 tokens x 32 heads x 128 bf16 (403 MB per tensor)
+@pytest.mark.parametrize("T_pad", [49160, 131072, 524288], ids=["c5-403MB", "sweep-1GB", "sweep-4GB"])
+def test_full_size_exchange_round_trip_and_sampled_map(T_pad):
+    # [1, T_pad, 32, 128] bf16 (8 KB per token): the c5 tensors (403 MB) and the
+    # 1 GB and 4 GB points of the standalone permute sweep, W = 8
     W, B, H, D = 8, 1, 32, 128
-    T_pad = 49160
     Tl, Hl = T_pad // W, H // W
-    g = torch.Generator(device="cuda").manual_seed(11)
+    g = torch.Generator(device="cuda").manual_seed(11 + T_pad)
     shards = [torch.randint(-32768, 32767, (B, Tl, H, D), dtype=torch.int16, device="cuda", generator=g)
               .view(torch.bfloat16) for _ in range(W)]
     heads = [torch.empty(B, T_pad, Hl, D, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
@@ -155,9 +156,13 @@ def test_full_size_exchange_round_trip_and_sampled_map():
     back = [torch.empty_like(s) for s in shards]
     sp.sp_gather_heads(heads, back, ws)
     for r in range(W):
-        assert torch.equal(back[r].view(torch.int16), shards[r].view(torch.int16))
-    # sampled tokens: the oracle's exchange of those tokens alone must match
-    t_sel = torch.tensor([0, 1, 777, 3000, Tl - 2, Tl - 1])
+        assert torch.equal(back[r].view(torch.int16), shards[r].view(torch.int16))  # gather(send(x)) == x
+    del back
+    # sampled tokens (the first and last two of every shard, and some in between):
+    # the oracle's exchange of those tokens alone must match
+    gen = torch.Generator().manual_seed(T_pad)
+    mid = torch.randint(2, Tl - 2, (6,), generator=gen)
+    t_sel = torch.cat([torch.tensor([0, 1]), mid, torch.tensor([Tl - 2, Tl - 1])])
     mini = [bytes_np(s[:, t_sel]) for s in shards]
     mini_heads = oracle.send_recv_heads(mini)
     for r in range(W):
@@ -165,6 +170,8 @@ def test_full_size_exchange_round_trip_and_sampled_map():
         assert np.array_equal(bytes_np(heads[r][:, rows]), mini_heads[r])
     torch.cuda.synchronize()
     assert sp.sp_workspace_status(ws)[0] == 0
+    del shards, heads
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("B,T,W,H,D,dtype", CASES)

@@ -51,3 +51,24 @@ def test_noalloc_exchange_rejects_more_ranks_than_its_scratch_holds():
     heads = [torch.zeros(1, 18, 1, 8, dtype=torch.bfloat16, device="cuda") for _ in range(9)]
     with pytest.raises(ValueError, match="static scratch"):
         sp.sp_send_recv_heads_noalloc(shards, heads)
+
+
+def test_noalloc_rejected_call_leaves_the_scratch_alone():
+    # A call rejected by the host-side argument checks returns its error before
+    # touching the shared array; the status word of the asynchronous call before
+    # it is then still there for the next call that reads it.
+    import ctypes
+    from sequence_video_dit_gb300._lib import lib, ptr_array
+    W, B, Tl, H, D = 4, 1, 96, 8, 64
+    shards = _shards(W, B, Tl, H, D, torch.bfloat16, seed=11)
+    want = [torch.empty(B, W * Tl, H // W, D, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+    got = [torch.empty_like(x) for x in want]
+    sp.sp_send_recv_heads(shards, want, sp.new_workspace())
+    assert sp.sp_send_recv_heads_noalloc(shards, got, read_status=False) is None
+    st = ctypes.c_int(-1)
+    rc = lib().sp_send_recv_heads_noalloc(ptr_array(shards), ptr_array(got), W, B, Tl, H, D, 3,
+                                          ctypes.byref(st), None)
+    assert rc == 3 and st.value == -1  # SP_ERR_INVALID_ARG (elt_bytes = 3); no status was read
+    assert sp.sp_send_recv_heads_noalloc(shards, got) == 0
+    for r in range(W):
+        assert torch.equal(got[r].view(torch.uint8), want[r].view(torch.uint8))
