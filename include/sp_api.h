@@ -305,26 +305,41 @@ SP_API int sp_attention(const void *const *q, const void *const *k, const void *
                  sp_mask_kind mask_kind, const uint8_t *mask, float scale, void *workspace,
                  size_t workspace_bytes, sp_stream_t stream);
 
-/* The head exchange fused into the attention (one GPU, token shards whose
- * length is a whole number of 128-row tiles).  sp_send_recv_heads only moves
- * each rank's heads of every source shard into one buffer; here the
- * attention's tile loads read them where they are: key tile j (rows
- * [128j, 128j+128) of the gathered sequence) comes from source shard
- * s = 128j / (Tk/W), rows 128j - s*(Tk/W), heads [r*Hl, (r+1)*Hl) for rank r.
- * The masks, the tiles and their order are those of sp_attention on the
- * exchanged tensors, so the result is the same bit for bit.
+/* The head exchange fused into the attention (one GPU): sp_send_recv_heads
+ * only moves each rank's heads of every source shard into one buffer; here
+ * the attention's tile loads read them where they are (sections 换头 and
+ * 直写: the data goes straight to its consumer, with no intermediate copy).
  *
- * shard_flags: SP_SHARD_KV -- k[s], v[s] are the W source-rank token shards
- * [B, Tk/W, H, D] (all H heads; strides kv_strides, or NULL for contiguous);
- * SP_SHARD_Q -- q[s], o[s] are token shards [B, Tq/W, H, D] read and written
- * in place (o[s] then receives every rank's heads of shard s, the layout
- * sp_gather_heads produces).  An operand without its flag is per rank as in
- * sp_attention: [B, T, H/W, D] views with their strides.
- * H is the total head count (H % W == 0).  A sharded operand needs
- * T % W == 0 and (T/W) % 128 == 0 (else SP_ERR_NOT_DIVISIBLE /
- * SP_ERR_UNSUPPORTED: use the exchange); bf16 with D = 64 or 128 only,
- * 16-byte aligned pointers and strides.  Mask, scale, workspace
- * (sp_attention_workspace_bytes with Hl = H/W) and status as sp_attention. */
+ * A sharded operand of T tokens (Tq for q/o, Tk for k/v) is given as its W
+ * source-rank token shards, Tl = ceil(T / W) tokens apart: shard s holds
+ * tokens [s*Tl, s*Tl + n_s) in its first n_s = clamp(T - s*Tl, 0, Tl) rows,
+ * all H heads ([B, >= n_s, H, D], strides as below).  These may be views of
+ * the caller's unpadded [B, T, H, D] tensor -- the last shards then stop at
+ * token T, and a shard with n_s = 0 may be NULL -- or padded [B, Tl, H, D]
+ * buffers passed with T = W*Tl.  Rows past n_s are never read or written, so
+ * no padding and no padding mask is needed; masks index real tokens
+ * (SP_MASK_KEY: [Tk], SP_MASK_FULL: [B, Tq, Tk]).
+ *
+ * Rank r's local head h is head r*Hl + h of every shard.  Its keys are
+ * visited as every shard's whole 128-row tiles (loaded by TMA from the
+ * shard), then "tail" tiles that gather the rows each shard has left,
+ * n_s % 128 of them, copied row by row; queries are tiled the same way and
+ * O rows go back to their shard.  Attention does not depend on the order of
+ * its keys, so only the rounding of the key sum differs from sp_attention on
+ * the exchanged (padded, key-masked) tensors; when Tl is a multiple of 128
+ * the tiles are exactly the exchanged layout's and the result is the same
+ * bit for bit.
+ *
+ * shard_flags: SP_SHARD_KV -- k[s], v[s] are shards (strides kv_strides, or
+ * NULL for contiguous [B, Tl, H, D]); SP_SHARD_Q -- q[s], o[s] are shards read
+ * and written in place (o[s] then receives every rank's heads of shard s, the
+ * layout sp_gather_heads produces).  An operand without its flag is per rank
+ * as in sp_attention: [B, T, H/W, D] views with their strides.
+ * H is the total head count (H % W == 0, else SP_ERR_HEADS_NOT_DIVISIBLE);
+ * bf16 with D = 64 or 128 only (else SP_ERR_UNSUPPORTED), 16-byte aligned
+ * pointers and strides (else SP_ERR_ALIGNMENT); Tk = 0 gives
+ * SP_ERR_UNSUPPORTED.  Scale, workspace (sp_attention_workspace_bytes with
+ * Hl = H/W and these Tq, Tk) and status as sp_attention. */
 #define SP_SHARD_KV 1
 #define SP_SHARD_Q 2
 SP_API int sp_attention_shards(const void *const *q, const void *const *k, const void *const *v, void *const *o,

@@ -321,11 +321,16 @@ def sp_attention(q, k, v, o, workspace: torch.Tensor, mask_kind: int = SP_MASK_N
 
 # ---------------------------------------------------------------- 还原
 def sp_attention_shards(q, k, v, o, workspace: torch.Tensor, shard_flags: int, mask_kind: int = SP_MASK_NONE,
-                        mask=None, scale: float = 0.0, stream=None):
-    """The head exchange fused into the attention: an operand with its flag in
-    ``shard_flags`` is the list of W source-rank token shards [B, T/W, H, D]
-    (views allowed, D contiguous) read -- or for o written -- in place;
-    without it, it is per rank as in sp_attention ([B, T, H/W, D] views)."""
+                        mask=None, scale: float = 0.0, stream=None, Tq: int | None = None, Tk: int | None = None):
+    """The head exchange fused into the attention.  An operand with its flag
+    in ``shard_flags`` is the list of the W source-rank token shards of its T
+    tokens (views allowed, D contiguous), read -- or for o written -- in
+    place: with Tl = ceil(T / W), shard s holds tokens [s*Tl, s*Tl + n_s) in
+    its first n_s = clamp(T - s*Tl, 0, Tl) rows, [B, >= n_s, H, D] (views of
+    the caller's [B, T, H, D] tensor, or padded [B, Tl, H, D] buffers).
+    ``Tq`` / ``Tk`` give T; by default the sum of the shards' lengths.
+    An operand without its flag is per rank as in sp_attention
+    ([B, T, H/W, D] views)."""
     W = len(q)
     if not (len(k) == len(v) == len(o) == W):
         raise SPValueError(3, "sp_attention_shards: q/k/v/o lists differ in length")
@@ -333,16 +338,35 @@ def sp_attention_shards(q, k, v, o, workspace: torch.Tensor, shard_flags: int, m
         if not t.is_cuda:
             raise SPValueError(3, "expected CUDA tensors")
     sq, skv = bool(shard_flags & SP_SHARD_Q), bool(shard_flags & SP_SHARD_KV)
-    B, tq, hq, D = q[0].shape
-    _, tk, hk, _ = k[0].shape
+    B, _, hq, D = q[0].shape
+    hk = k[0].shape[2]
     H = hq if sq else hq * W
     if (hk if skv else hk * W) != H:
         raise SPValueError(3, "sp_attention_shards: q and k disagree on the head count")
-    Tq = tq * W if sq else tq
-    Tk = tk * W if skv else tk
-    for lst, shape in ((q, q[0].shape), (o, q[0].shape), (k, k[0].shape), (v, k[0].shape)):
+
+    def tokens(lst, sharded, T, name):
+        if not sharded:
+            T = lst[0].shape[1] if T is None else T
+            want = [T] * W
+        else:
+            T = sum(t.shape[1] for t in lst) if T is None else T
+            Tl = -(-T // W)
+            want = [min(max(T - s * Tl, 0), Tl) for s in range(W)]
+            if T and lst[0].shape[1] != Tl:
+                raise SPValueError(3, f"sp_attention_shards: {name} shard 0 must hold ceil({T}/{W}) = {Tl} rows")
+        for t, n in zip(lst, want):
+            if t.shape[1] < n or (not sharded and t.shape[1] != n):
+                raise SPValueError(3, f"sp_attention_shards: a {name} tensor holds {t.shape[1]} rows, needs {n}")
+        return T
+
+    Tq = tokens(q, sq, Tq, "q")
+    tokens(o, sq, Tq, "o")
+    Tk = tokens(k, skv, Tk, "k")
+    tokens(v, skv, Tk, "v")
+    for lst in (q, o, k, v):
         for t in lst:
-            if tuple(t.shape) != tuple(shape) or t.dtype != q[0].dtype or t.stride() != lst[0].stride():
+            if (t.shape[0], t.shape[2], t.shape[3]) != (lst[0].shape[0], lst[0].shape[2], lst[0].shape[3]) or \
+                    t.dtype != q[0].dtype or t.stride() != lst[0].stride() or t.shape[0] != B or t.shape[3] != D:
                 raise SPValueError(3, "sp_attention_shards: inconsistent shapes, dtypes or strides")
     if tuple(k[0].stride()) != tuple(v[0].stride()):
         raise SPValueError(3, "sp_attention_shards: k and v must share strides")

@@ -169,12 +169,10 @@ int sp_attention_shards(const void *const *q, const void *const *k, const void *
     if (H % W != 0)
         return set_error(SP_ERR_HEADS_NOT_DIVISIBLE, "sp_attention_shards: H=%d is not divisible by W=%d", H, W);
     const bool sq = (shard_flags & SP_SHARD_Q) != 0, skv = (shard_flags & SP_SHARD_KV) != 0;
-    if ((sq && Tq % W != 0) || (skv && Tk % W != 0))
-        return set_error(SP_ERR_NOT_DIVISIBLE, "sp_attention_shards: total_tokens is not divisible by world_size=%d", W);
-    if ((sq && (Tq / W) % 128 != 0) || (skv && (Tk / W) % 128 != 0))
-        return set_error(SP_ERR_UNSUPPORTED,
-                         "sp_attention_shards: token shards of %d / %d rows are not whole 128-row tiles", sq ? Tq / W : 0,
-                         skv ? Tk / W : 0);
+    // a sharded operand of T tokens: shards of Tl = ceil(T / W) tokens, the
+    // last ones short of real rows when T % W != 0 (the pages' padded
+    // partition; pad rows need not exist)
+    const int q_tl = sq ? (int)(((int64_t)Tq + W - 1) / W) : 0, kv_tl = skv ? (int)(((int64_t)Tk + W - 1) / W) : 0;
     if (dtype != SP_BF16 || (D != 64 && D != 128))
         return set_error(SP_ERR_UNSUPPORTED, "sp_attention_shards: bf16 with D = 64 or 128 only");
     if (mask_kind != SP_MASK_NONE && mask_kind != SP_MASK_KEY && mask_kind != SP_MASK_FULL)
@@ -196,14 +194,16 @@ int sp_attention_shards(const void *const *q, const void *const *k, const void *
     a.Hl = H / W;
     a.D = D;
     a.dtype = dtype;
-    a.q_shard_rows = sq ? Tq / W : 0;
-    a.kv_shard_rows = skv ? Tk / W : 0;
-    default_strides(a.qs, q_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
-    default_strides(a.ks, kv_strides, skv ? Tk / W : Tk, skv ? H : a.Hl, D);
-    default_strides(a.os, o_strides, sq ? Tq / W : Tq, sq ? H : a.Hl, D);
+    a.q_shard_rows = q_tl;
+    a.kv_shard_rows = kv_tl;
+    default_strides(a.qs, q_strides, sq ? q_tl : Tq, sq ? H : a.Hl, D);
+    default_strides(a.ks, kv_strides, skv ? kv_tl : Tk, skv ? H : a.Hl, D);
+    default_strides(a.os, o_strides, sq ? q_tl : Tq, sq ? H : a.Hl, D);
     if ((int64_t)W * B * (H / W) * Tq == 0) return SP_OK;  // nothing to compute (empty tensors may be null)
     for (int r = 0; r < W; r++) {
-        if (!q[r] || !o[r] || (Tk > 0 && (!k[r] || !v[r])))
+        // a shard with no real rows is never read and may be NULL
+        const bool need_q = !sq || (int64_t)r * q_tl < Tq, need_kv = Tk > 0 && (!skv || (int64_t)r * kv_tl < Tk);
+        if ((need_q && (!q[r] || !o[r])) || (need_kv && (!k[r] || !v[r])))
             return set_error(SP_ERR_INVALID_ARG, "sp_attention_shards: null tensor %d", r);
         a.q[r] = q[r];
         a.k[r] = k[r];

@@ -14,9 +14,11 @@ struct AttnArgs {
     sp_dtype dtype;
     int64_t qs[3], ks[3], os[3];  // batch, token, head strides in elements
     // 0: q/o (resp. k/v) are per-rank [B, T, Hl, D] tensors; > 0: they are the
-    // W source-rank token shards [B, shard_rows, W*Hl, D] (rank r's heads at
-    // [r*Hl, (r+1)*Hl)), read and written in place -- the exchange fused into
-    // the attention.  shard_rows is a multiple of the 128-row tile.
+    // W source-rank token shards of the T = Tq (Tk) real tokens, shard_rows =
+    // ceil(T / W) tokens apart: shard s holds tokens [s*shard_rows, ...) in its
+    // first clamp(T - s*shard_rows, 0, shard_rows) rows, all H = W*Hl heads
+    // (rank r's at [r*Hl, (r+1)*Hl)), read and written in place -- the
+    // exchange fused into the attention.
     int q_shard_rows, kv_shard_rows;
     int mask_kind;
     const uint8_t *mask;

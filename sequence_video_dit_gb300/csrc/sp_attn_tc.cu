@@ -33,8 +33,10 @@
 // into key pieces, and a last, partial wave of items is cut likewise; the
 // pieces' fp32 partials are merged by LSE in attn_merge_kernel.
 // Operands are either each rank's tensors or, for the exchange fused into
-// the attention, the source ranks' token shards (tile_source picks the shard
-// a 128-row tile lives in).
+// the attention, the source ranks' token shards (Tiling): every shard's whole
+// 128-row tiles come by TMA from the shard, and the rows the shards have
+// left over are gathered into tail tiles that the producer warp copies row
+// by row into the same swizzled layout.
 //
 // Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
 // SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
@@ -66,14 +68,35 @@ struct Cfg {
     static constexpr int SMEM_ALLOC = BYTES + 1024;  // + slack to align the base to 1024
 };
 
+// How the 128-row tiles of one operand map onto its memory.  A per-rank
+// tensor (sharded == 0): tile j is rows [128 j, 128 j + 128).  W source token
+// shards (sharded != 0): global token g lives in shard g / Tl at row g % Tl,
+// and shard s holds n_s real rows.  The tiles are every shard's whole
+// 128-row tiles in shard order (shard s owns tiles [full0[s], full0[s+1])),
+// then "tail" tiles that gather the rows each shard has left after its whole
+// tiles, n_s % 128 of them, in shard order (shard s's leftovers are tail
+// slots [tail0[s], tail0[s+1])); slots past tail0[W] hold no token.  With
+// Tl a multiple of 128 and every shard full there are no tail tiles and tile j
+// is global rows [128 j, 128 j + 128), the order of the exchanged layout.
+struct Tiling {
+    int sharded;
+    int Tl;
+    int full0[SP_MAX_RANKS + 1];
+    int tail0[SP_MAX_RANKS + 1];
+};
+
 struct alignas(128) TcParams {
     CUtensorMap tq[SP_MAX_RANKS], tk[SP_MAX_RANKS], tv[SP_MAX_RANKS], to[SP_MAX_RANKS];
     int W, B, Tq, Tk, Hl;
     int n_qpairs, n_kv, n_split, kv_per_split;
     int n_full;  // SPLIT launches: work items [0, n_full) run whole, the rest in n_split key pieces
-    // > 0: Q/O (resp. K/V) maps are per source token shard of this many rows,
-    // addressed with head r * Hl + h; a 128-row tile never straddles shards
-    int q_shard_rows, kv_shard_rows;
+    // Tilings of Q/O and of K/V.  A sharded operand's maps are per source
+    // token shard, addressed with head r * Hl + h; tail tiles are copied by
+    // the producer warp from the raw pointers below (strides in elements).
+    Tiling qtl, ktl;
+    const uint8_t *qptr[SP_MAX_RANKS], *kptr[SP_MAX_RANKS], *vptr[SP_MAX_RANKS];
+    uint8_t *optr[SP_MAX_RANKS];
+    int64_t qs[3], ks[3], os[3];
     float scale_log2;
     int mask_kind, mask_vec4;
     const uint8_t *mask;
@@ -104,6 +127,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+// Raises the transaction count of the current phase without an arrival.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -348,27 +383,130 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
     }
 }
 
-// Where a 128-row tile starting at global row `row` of rank r's head h lives:
-// the rank's own tensor (shard_rows == 0), or token shard row / shard_rows of
-// the source ranks, at head r * Hl + h.  Rows past the last shard (a ragged
-// query tile) map into the last shard past its end, where TMA loads read
-// zeros and stores are clipped.
-__device__ __forceinline__ void tile_source(int shard_rows, int row, int r, int h, int Hl, int W, int &map,
-                                            int &head, int &srow) {
-    if (shard_rows <= 0) {
+// Whole tile j of a sharded operand: its shard s and first row; false when j
+// is a tail tile (or past the last tile).
+__device__ __forceinline__ bool tiling_whole(const Tiling &t, int W, int j, int &s, int &row) {
+    if (j >= t.full0[W]) return false;
+    int q = 0;
+    while (q + 1 < W && j >= t.full0[q + 1]) q++;
+    s = q;
+    row = (j - t.full0[q]) * 128;
+    return true;
+}
+// Tail slot idx (counted over every shard's leftover rows): its shard s and
+// row; false past the last leftover row.
+__device__ __forceinline__ bool tiling_tail(const Tiling &t, int W, int idx, int &s, int &row) {
+    if (idx < 0 || idx >= t.tail0[W]) return false;
+    int q = 0;
+    while (q + 1 < W && idx >= t.tail0[q + 1]) q++;
+    s = q;
+    row = (t.full0[q + 1] - t.full0[q]) * 128 + (idx - t.tail0[q]);
+    return true;
+}
+// Where tile j of rank r's local head h comes from when TMA can load it:
+// the rank's own tensor (map r, head h, rows [128 j, 128 j + 128)) or a
+// whole tile of source shard s (map s, head r * Hl + h).  False for a tail
+// tile, which the producer warp assembles row by row.
+__device__ __forceinline__ bool tile_src(const Tiling &t, int W, int j, int r, int h, int Hl, int &map, int &head,
+                                         int &row) {
+    if (!t.sharded) {
         map = r;
         head = h;
-        srow = row;
+        row = j * 128;
+        return true;
+    }
+    head = r * Hl + h;
+    return tiling_whole(t, W, j, map, row);
+}
+// Global token of row e of tile j, or -1 when the slot holds no token.
+__device__ __forceinline__ int tile_token(const Tiling &t, int W, int j, int e) {
+    if (!t.sharded) return j * 128 + e;
+    int s, row;
+    if (tiling_whole(t, W, j, s, row)) return s * t.Tl + row + e;
+    if (tiling_tail(t, W, (j - t.full0[W]) * 128 + e, s, row)) return s * t.Tl + row;
+    return -1;
+}
+
+// Tail tile tt of a sharded operand into the 128-byte-swizzled tile at
+// shared address dst (the layout a TMA box writes: 64-column blocks 16 KB
+// apart, row e at e * 128, 16-byte chunk c at (c ^ (e & 7)) * 16), by all 32
+// lanes of the calling warp with 16-byte copies; slots that hold no token are
+// zero-filled.  base: the W shards; st: batch, token, head strides (elements).
+template <int D>
+__device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, int tt, const uint8_t *const *base,
+                                          const int64_t *st, int b, int head, int lane) {
+    constexpr int CPR = D / 8;     // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;  // rows per pass of the warp
+    const int c = lane % CPR;
+    for (int e = lane / CPR; e < 128; e += RPI) {
+        int s = 0, row = 0;
+        const bool ok = tiling_tail(t, W, tt * 128 + e, s, row);
+        const uint8_t *src =
+            ok ? base[s] + ((int64_t)b * st[0] + (int64_t)row * st[1] + (int64_t)head * st[2]) * 2 + c * 16 : base[0];
+        const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
+        cp_async_16(d, src, ok ? 16u : 0u);
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();  // the tensor core (async proxy) reads what these copies wrote
+}
+
+// Visibility bits of tail key tile tt for this thread's query row (global
+// token q_row, or >= Tq for a slot without a query): slots past the last
+// leftover row are never visible.
+__device__ __forceinline__ void tail_words(const TcParams &p, int b, int q_row, int tt, int lane, uint32_t w[4]) {
+    const Tiling &t = p.ktl;
+    const int nvalid = min(max(t.tail0[p.W] - tt * 128, 0), 128);
+    if (p.mask_kind == SP_MASK_KEY) {
+        // warp-cooperative: lane covers slots 4*lane .. +3
+        uint32_t nib = 0;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            int s, row;
+            if (tiling_tail(t, p.W, tt * 128 + 4 * lane + e, s, row) && p.mask[s * t.Tl + row]) nib |= 1u << e;
+        }
+        uint32_t word = nib << (4 * (lane & 7));
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        word |= __shfl_xor_sync(0xffffffffu, word, 4);
+        w[0] = __shfl_sync(0xffffffffu, word, 0);
+        w[1] = __shfl_sync(0xffffffffu, word, 8);
+        w[2] = __shfl_sync(0xffffffffu, word, 16);
+        w[3] = __shfl_sync(0xffffffffu, word, 24);
         return;
     }
-    const int s = min(row / shard_rows, W - 1);
-    map = s;
-    head = r * Hl + h;
-    srow = row - s * shard_rows;
+    if (p.mask_kind == SP_MASK_FULL && q_row < p.Tq) {
+        const uint8_t *mrow = p.mask + ((int64_t)b * p.Tq + q_row) * p.Tk;
+        for (int g = 0; g < 4; g++) w[g] = 0u;
+        for (int e = 0; e < nvalid; e++) {
+            int s, row;
+            tiling_tail(t, p.W, tt * 128 + e, s, row);
+            if (mrow[s * t.Tl + row]) w[e >> 5] |= 1u << (e & 31);
+        }
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        const int n = nvalid - 32 * g;
+        w[g] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+    }
+}
+
+// Visibility bits of key tile j (any tiling) for this thread's query row.
+__device__ __forceinline__ void key_words(const TcParams &p, int b, int q_row, int j, int lane, uint32_t w[4]) {
+    int s, row;
+    if (!p.ktl.sharded) {
+        mask_words(p, b, q_row, j * 128, lane, w);
+    } else if (tiling_whole(p.ktl, p.W, j, s, row)) {
+        mask_words(p, b, q_row, s * p.ktl.Tl + row, lane, w);  // 128 consecutive real tokens
+    } else {
+        tail_words(p, b, q_row, j - p.ktl.full0[p.W], lane, w);
+    }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool SPLIT>
+// TILED: some operand is a set of token shards (see Tiling); otherwise every
+// operand is a per-rank tensor and the tile arithmetic is the plain one.
+template <int D, bool SPLIT, bool TILED>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
     constexpr int NSLOT = C::NSLOT;  // ring slots
@@ -455,17 +593,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (warp == 8) {
         // ---------------------------------------------------------- TMA producer
-        if (lane == 0 && nkv > 0) {
+        if (!TILED && lane == 0 && nkv > 0) {
             prefetch_tmap(&p.tq[r]);
             prefetch_tmap(&p.tk[r]);
             prefetch_tmap(&p.tv[r]);
             mbar_arrive_expect_tx(&bar_q, 2 * C::TILE);
             for (int i = 0; i < 2; i++) {
-                int qmap, qhead, qrow;
-                tile_source(p.q_shard_rows, qp * 256 + i * 128, r, h, p.Hl, p.W, qmap, qhead, qrow);
                 for (int db = 0; db < C::DB; db++) {
                     const uint32_t dst = sbase + C::Q_OFF + i * C::TILE + db * 16384;
-                    tma_load_4d(&bar_q, &p.tq[qmap], dst, db * 64, qhead, qrow, b);
+                    tma_load_4d(&bar_q, &p.tq[r], dst, db * 64, h, qp * 256 + i * 128, b);
                 }
             }
             // load n: K of key tile n/2 (n even) or V (n odd) into slot n % NSLOT
@@ -478,12 +614,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (use > 0 && !wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status))
                     break;
                 mbar_arrive_expect_tx(&bar_full[slot], SLOT);
-                int kmap, khead, kshrow;
-                tile_source(p.kv_shard_rows, key_tile(n >> 1) * 128, r, h, p.Hl, p.W, kmap, khead, kshrow);
-                const CUtensorMap *m = (n & 1) ? &p.tv[kmap] : &p.tk[kmap];
+                const CUtensorMap *m = (n & 1) ? &p.tv[r] : &p.tk[r];
+                const int krow = key_tile(n >> 1) * 128;
                 for (int db = 0; db < C::DB; db++)
-                    tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, khead,
-                                kshrow, b);
+                    tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64, h, krow,
+                                b);
             }
             // Before the CTA may exit, every load it issued has landed: wait
             // for the newest load of every slot (older ones were consumed
@@ -494,6 +629,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (int slot = 0; slot < NSLOT && slot < n; slot++) {
                 const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
                 wait_drain(&bar_full[slot], (uint32_t)(last / NSLOT) & 1u);
+            }
+        } else if (TILED && nkv > 0) {
+            // The whole warp runs the loop: lane 0 waits and issues the TMA
+            // loads of whole tiles; a tail tile is copied by all 32 lanes and
+            // then announced by one plain arrival.
+            if (lane < p.W) {
+                prefetch_tmap(&p.tq[lane]);
+                prefetch_tmap(&p.tk[lane]);
+                prefetch_tmap(&p.tv[lane]);
+            }
+            int qmap[2], qhead[2], qrow[2];
+            bool qwhole[2];
+            uint32_t qbytes = 0;
+            for (int i = 0; i < 2; i++) {
+                qwhole[i] = tile_src(p.qtl, p.W, 2 * qp + i, r, h, p.Hl, qmap[i], qhead[i], qrow[i]);
+                if (qwhole[i]) qbytes += C::TILE;
+            }
+            if (lane == 0) {
+                if (qbytes) mbar_expect_tx(&bar_q, qbytes);
+                for (int i = 0; i < 2; i++)
+                    if (qwhole[i])
+                        for (int db = 0; db < C::DB; db++)
+                            tma_load_4d(&bar_q, &p.tq[qmap[i]], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64,
+                                        qhead[i], qrow[i], b);
+            }
+            for (int i = 0; i < 2; i++)
+                if (!qwhole[i])
+                    fill_tail<D>(sbase + C::Q_OFF + i * C::TILE, p.qtl, p.W, 2 * qp + i - p.qtl.full0[p.W], p.qptr,
+                                 p.qs, b, qhead[i], lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_q);
+            const int stall = *p.kv_stall;  // 0 in normal use
+            const int nloads = stall > 0 ? min(2 * nkv, stall - 1) : 2 * nkv;
+            int n = 0;
+            for (; n < nloads; n++) {
+                const int slot = n % NSLOT;
+                const int use = n / NSLOT;
+                bool ok = true;
+                if (use > 0 && lane == 0)
+                    ok = wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+                const int j = key_tile(n >> 1);
+                int kmap, khead, krow;
+                if (tile_src(p.ktl, p.W, j, r, h, p.Hl, kmap, khead, krow)) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bar_full[slot], SLOT);
+                        const CUtensorMap *m = (n & 1) ? &p.tv[kmap] : &p.tk[kmap];
+                        for (int db = 0; db < C::DB; db++)
+                            tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64,
+                                        khead, krow, b);
+                    }
+                } else {
+                    fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.full0[p.W],
+                                 (n & 1) ? p.vptr : p.kptr, p.ks, b, khead, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_full[slot]);
+                }
+            }
+            if (lane == 0) {
+                wait_drain(&bar_q, 0);
+                for (int slot = 0; slot < NSLOT && slot < n; slot++) {
+                    const int last = slot + ((n - 1 - slot) / NSLOT) * NSLOT;
+                    wait_drain(&bar_full[slot], (uint32_t)(last / NSLOT) & 1u);
+                }
             }
         }
         __syncwarp();
@@ -597,7 +796,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int i = warp >> 2;       // query tile of the pair
         const int quarter = warp & 3;  // TMEM lane quarter
         const int row = quarter * 32 + lane;
-        const int q_row = qp * 256 + i * 128 + row;
+        // global query token of this thread's row (>= Tq: the slot holds none)
+        int q_row = qp * 256 + i * 128 + row;
+        if (TILED) {
+            q_row = tile_token(p.qtl, p.W, 2 * qp + i, row);
+            if (q_row < 0) q_row = p.Tq;
+        }
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS_me = tbase + lane_off + (uint32_t)(i * 128);
         const uint32_t tO_me = tbase + lane_off + 256u + (uint32_t)(i * 128);
@@ -607,7 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // Visibility bits of the tile to come are fetched while the tensor core
         // still works on it, never between S arriving and P leaving.
         uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (nkv > 0) mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
+        if (nkv > 0) {
+            if (TILED) key_words(p, b, q_row, key_tile(0), lane, w);
+            else mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
+        }
         for (int jj = 0; jj < nkv; jj++) {
             const bool s_ok = wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status);
             if (!__all_sync(0xffffffffu, s_ok)) {  // leave together: the loop body is warp-collective
@@ -676,7 +883,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bar_pf[i]);
-            if (jj + 1 < nkv) mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
+            if (jj + 1 < nkv) {
+                if (TILED) key_words(p, b, q_row, key_tile(jj + 1), lane, w);
+                else mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
+            }
         }
         // the epilogue has a 128-thread barrier: the tile's four warps decide together
         const bool epi = named_bar_and(1 + i, 128, ok && !*abort_flag);
@@ -691,7 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             if (have) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                if (!SPLIT || piece < 0) {
+                int omap = r, ohead = h, orow = qp * 256 + i * 128;
+                const bool whole = !TILED || tile_src(p.qtl, p.W, 2 * qp + i, r, h, p.Hl, omap, ohead, orow);
+                if ((!SPLIT || piece < 0) && whole) {
                     uint8_t *tile = sgen + C::Q_OFF + i * C::TILE;
 #pragma unroll
                     for (int db = 0; db < C::DB; db++) {
@@ -720,13 +932,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     fence_proxy_async_smem();
                     named_bar_sync(1 + i, 128);
                     if (quarter == 0 && lane == 0) {
-                        int omap, ohead, orow;
-                        tile_source(p.q_shard_rows, qp * 256 + i * 128, r, h, p.Hl, p.W, omap, ohead, orow);
                         for (int db = 0; db < C::DB; db++)
                             tma_store_4d(&p.to[omap], sbase + C::Q_OFF + i * C::TILE + db * 16384, db * 64, ohead,
                                          orow, b);
                         bulk_commit();
                         bulk_wait_read0();
+                    }
+                } else if (TILED && (!SPLIT || piece < 0)) {
+                    // tail query tile: every thread stores its own row, if it holds a token
+                    int s = 0, srow = 0;
+                    const bool mine =
+                        q_row < p.Tq && tiling_tail(p.qtl, p.W, (2 * qp + i - p.qtl.full0[p.W]) * 128 + row, s, srow);
+                    uint8_t *orow_ptr = mine ? p.optr[s] + ((int64_t)b * p.os[0] + (int64_t)srow * p.os[1] +
+                                                            (int64_t)(r * p.Hl + h) * p.os[2]) * 2
+                                             : nullptr;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; cc++) {
+                        uint32_t o[32];
+                        if (nkv > 0) {
+                            tmem_ld_x32(tO_me + cc * 32, o);  // warp-collective: every lane loads
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; e++) o[e] = 0u;
+                        }
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; e++)
+                            pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                        if (mine) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow_ptr + cc * 64);
+#pragma unroll
+                            for (int u = 0; u < 4; u++)
+                                dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                        }
                     }
                 } else {
                     const int64_t prow = ((witem - p.n_full) * p.n_split + piece) * 256 + i * 128 + row;
@@ -762,7 +1000,7 @@ struct MergeParams {
     void *o[SP_MAX_RANKS];
     int64_t os[3];
     int W, B, Tq, Hl, D, n_qpairs, n_split, n_full, n_pieced;
-    int q_shard_rows;  // > 0: o[s] are token shards (see TcParams)
+    Tiling qtl;  // sharded: o[s] are token shards (see TcParams)
     const float *part_o, *part_lse;
 };
 
@@ -781,8 +1019,21 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
     t /= a.Hl;
     const int b = (int)(t % a.B);
     const int r = (int)(t / a.B);
-    const int q = qp * 256 + row;
-    if (q >= a.Tq) return;
+    int omap = r, ohead = h, orow = qp * 256 + row;
+    if (!a.qtl.sharded) {
+        if (orow >= a.Tq) return;
+    } else {
+        const int j = qp * 2 + (row >> 7), e = row & 127;
+        int s, srow;
+        if (tiling_whole(a.qtl, a.W, j, s, srow)) {
+            srow += e;
+        } else if (!tiling_tail(a.qtl, a.W, (j - a.qtl.full0[a.W]) * 128 + e, s, srow)) {
+            return;  // the slot holds no query
+        }
+        omap = s;
+        ohead = r * a.Hl + h;
+        orow = srow;
+    }
     const int64_t item = pi;  // partials are indexed by pieced item
     float L = -INFINITY;
     for (int s = 0; s < a.n_split; s++) L = fmaxf(L, a.part_lse[(item * a.n_split + s) * 256 + row]);
@@ -800,12 +1051,6 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    int omap = r, ohead = h, orow = q;
-    if (a.q_shard_rows > 0) {
-        omap = q / a.q_shard_rows;
-        ohead = r * a.Hl + h;
-        orow = q - omap * a.q_shard_rows;
-    }
     __nv_bfloat16 *O = (__nv_bfloat16 *)a.o[omap] + b * a.os[0] + (int64_t)orow * a.os[1] + ohead * a.os[2];
 #pragma unroll
     for (int j = 0; j < NJ; j++) O[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
@@ -838,6 +1083,26 @@ static int encode_map(CUtensorMap *m, const void *base, int D, int Hl, int T, in
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rc != CUDA_SUCCESS) return set_error(SP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)rc);
     return SP_OK;
+}
+
+// Real rows of shard s of an operand of T tokens in shards of Tl (the
+// operand's own T rows when it is not sharded, Tl == 0).
+static int map_rows(int Tl, int T, int s) {
+    if (Tl <= 0) return T;
+    const int64_t n = (int64_t)T - (int64_t)s * Tl;
+    return (int)(n < 0 ? 0 : (n > Tl ? Tl : n));
+}
+
+static void make_tiling(Tiling &t, int Tl, int T, int W) {
+    memset(&t, 0, sizeof(t));
+    if (Tl <= 0) return;
+    t.sharded = 1;
+    t.Tl = Tl;
+    for (int s = 0; s < W; s++) {
+        const int n = map_rows(Tl, T, s);
+        t.full0[s + 1] = t.full0[s] + n / 128;
+        t.tail0[s + 1] = t.tail0[s] + n % 128;
+    }
 }
 
 // Work decomposition.  A work item is one (rank, batch, head, query pair); a
@@ -923,14 +1188,14 @@ bool attn_tc_supported(const AttnArgs &a) {
     return true;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool TILED>
 static int launch_tc_t(const tc::TcParams &prm, unsigned grid, cudaStream_t st) {
     // the shared-memory opt-in is a per-device attribute of each instance: set
     // once per device (a bit per device; a racing second set is harmless)
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     SP_CUDA_CHECK(cudaGetDevice(&dev));
-    auto kern = tc::attn_tc_kernel<D, SPLIT>;
+    auto kern = tc::attn_tc_kernel<D, SPLIT, TILED>;
     const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
     if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
         SP_CUDA_CHECK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Cfg<D>::SMEM_ALLOC));
@@ -949,17 +1214,33 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     if (di.cc_major != 10) return set_error(SP_ERR_UNSUPPORTED, "tcgen05 path needs a Blackwell (sm_10x) device");
     static thread_local tc::TcParams prm;  // 4+ KB: keep it off the stack
     memset(&prm, 0, sizeof(prm));
-    // per-rank tensors: [B, T, Hl, D]; token shards: [B, shard_rows, W*Hl, D]
-    const int qh = a.q_shard_rows > 0 ? a.W * a.Hl : a.Hl, qt = a.q_shard_rows > 0 ? a.q_shard_rows : a.Tq;
-    const int kh = a.kv_shard_rows > 0 ? a.W * a.Hl : a.Hl, kt = a.kv_shard_rows > 0 ? a.kv_shard_rows : a.Tk;
+    // per-rank tensors: [B, T, Hl, D]; token shards: [B, n_s, W*Hl, D], shard s
+    // holding its n_s real rows (maps end there: a shard may be a view that
+    // stops at the caller's last token)
+    tc::make_tiling(prm.qtl, a.q_shard_rows, a.Tq, a.W);
+    tc::make_tiling(prm.ktl, a.kv_shard_rows, a.Tk, a.W);
+    const int qh = a.q_shard_rows > 0 ? a.W * a.Hl : a.Hl, kh = a.kv_shard_rows > 0 ? a.W * a.Hl : a.Hl;
     for (int r = 0; r < a.W; r++) {
-        if ((rc = tc::encode_map(&prm.tq[r], a.q[r], a.D, qh, qt, a.B, a.qs))) return rc;
-        if ((rc = tc::encode_map(&prm.tk[r], a.k[r], a.D, kh, kt, a.B, a.ks))) return rc;
-        if ((rc = tc::encode_map(&prm.tv[r], a.v[r], a.D, kh, kt, a.B, a.ks))) return rc;
-        if ((rc = tc::encode_map(&prm.to[r], a.o[r], a.D, qh, qt, a.B, a.os))) return rc;
+        const int qt = tc::map_rows(a.q_shard_rows, a.Tq, r), kt = tc::map_rows(a.kv_shard_rows, a.Tk, r);
+        // a shard with no rows is never read: its map repeats shard 0's
+        const int rq = qt > 0 ? r : 0, rk = kt > 0 ? r : 0;
+        const int nq = qt > 0 ? qt : tc::map_rows(a.q_shard_rows, a.Tq, 0);
+        const int nk = kt > 0 ? kt : tc::map_rows(a.kv_shard_rows, a.Tk, 0);
+        if ((rc = tc::encode_map(&prm.tq[r], a.q[rq], a.D, qh, nq, a.B, a.qs))) return rc;
+        if ((rc = tc::encode_map(&prm.tk[r], a.k[rk], a.D, kh, nk, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.tv[r], a.v[rk], a.D, kh, nk, a.B, a.ks))) return rc;
+        if ((rc = tc::encode_map(&prm.to[r], a.o[rq], a.D, qh, nq, a.B, a.os))) return rc;
+        prm.qptr[r] = (const uint8_t *)a.q[r];
+        prm.kptr[r] = (const uint8_t *)a.k[r];
+        prm.vptr[r] = (const uint8_t *)a.v[r];
+        prm.optr[r] = (uint8_t *)a.o[r];
     }
-    prm.q_shard_rows = a.q_shard_rows;
-    prm.kv_shard_rows = a.kv_shard_rows;
+    for (int i = 0; i < 3; i++) {
+        prm.qs[i] = a.qs[i];
+        prm.ks[i] = a.ks[i];
+        prm.os[i] = a.os[i];
+    }
+    const bool tiled = a.q_shard_rows > 0 || a.kv_shard_rows > 0;
     tc::SplitPlan sp = tc::plan_split(a.W, a.B, a.Tq, a.Tk, a.Hl, a.D, di.num_sms);
     if (sp.n_split > 1 && (a.extra == nullptr || a.extra_bytes < sp.extra_bytes)) {
         sp.n_split = 1;
@@ -981,7 +1262,10 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     prm.scale_log2 = a.scale * 1.4426950408889634f;
     prm.mask_kind = a.mask_kind;
     prm.mask = a.mask;
-    prm.mask_vec4 = (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0) ? 1 : 0;
+    // 4-byte mask reads need 4-aligned key runs: every whole key tile of a
+    // sharded K/V starts at a multiple of the shard length
+    prm.mask_vec4 =
+        (a.mask && ((uintptr_t)a.mask & 3) == 0 && (a.Tk & 3) == 0 && (a.kv_shard_rows & 3) == 0) ? 1 : 0;
     prm.status = &a.ws->status;
     prm.kv_stall = &a.ws->kv_stall;
     const int64_t grid = sp.n_split > 1 ? (int64_t)sp.n_full + (int64_t)sp.n_pieced * sp.n_split
@@ -991,8 +1275,10 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
     if (sp.n_split > 1) {
         prm.part_o = reinterpret_cast<float *>(a.extra);
         prm.part_lse = prm.part_o + (size_t)sp.n_pieced * sp.n_split * 256 * a.D;
-        rc = (a.D == 64) ? launch_tc_t<64, true>(prm, (unsigned)grid, st)
-                         : launch_tc_t<128, true>(prm, (unsigned)grid, st);
+        rc = (a.D == 64) ? (tiled ? launch_tc_t<64, true, true>(prm, (unsigned)grid, st)
+                                  : launch_tc_t<64, true, false>(prm, (unsigned)grid, st))
+                         : (tiled ? launch_tc_t<128, true, true>(prm, (unsigned)grid, st)
+                                  : launch_tc_t<128, true, false>(prm, (unsigned)grid, st));
         if (rc) return rc;
         tc::MergeParams mp;
         memset(&mp, 0, sizeof(mp));
@@ -1007,7 +1293,7 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         mp.n_split = sp.n_split;
         mp.n_full = sp.n_full;
         mp.n_pieced = sp.n_pieced;
-        mp.q_shard_rows = a.q_shard_rows;
+        mp.qtl = prm.qtl;
         mp.part_o = prm.part_o;
         mp.part_lse = prm.part_lse;
         const int64_t rows = (int64_t)sp.n_pieced * 256;
@@ -1016,8 +1302,11 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);
         return check_launch("sp_attention(merge)");
     }
-    if (a.D == 64) return launch_tc_t<64, false>(prm, (unsigned)grid, st);
-    return launch_tc_t<128, false>(prm, (unsigned)grid, st);
+    if (a.D == 64)
+        return tiled ? launch_tc_t<64, false, true>(prm, (unsigned)grid, st)
+                     : launch_tc_t<64, false, false>(prm, (unsigned)grid, st);
+    return tiled ? launch_tc_t<128, false, true>(prm, (unsigned)grid, st)
+                 : launch_tc_t<128, false, false>(prm, (unsigned)grid, st);
 }
 
 }  // namespace sp

@@ -41,12 +41,17 @@ and no mask is needed.
 (sp_attention_shards): the operands that would go through sp_send_recv_heads
 are handed over as the W token shards and each attention tile is loaded from
 its source shard, O is written into token-shard layout, so no exchange kernel
-runs.  It needs shards of whole 128-row tiles (T_pad / W a multiple of 128)
-and the tensor-core kernel (bf16, D = 64 or 128).  With ``fused=False`` the
-shards are the W rank buffers sp_tile (or sp_tile_2d) fills and
-sp_gather_output (sp_gather_2d) assembles the output; with ``fused=True`` they
-are views of the caller's tensors and nothing is copied at all (T % W == 0).
-Either way the output equals the staged step's bit for bit.
+runs.  It needs the tensor-core kernel (bf16, D = 64 or 128).  With
+``fused=False`` the shards are the W rank buffers sp_tile (or sp_tile_2d)
+fills and sp_gather_output (sp_gather_2d) assembles the output; with
+``fused=True`` they are views of the caller's tensors, the last ones short of
+the pad rows when T % W != 0, and nothing is copied or padded at all: pad
+keys and pad queries are simply never read (no padding mask is needed; a
+user mask is read as the caller's (B, T, T) mask).  When every shard is a
+whole number of 128-row tiles the output equals the staged step's bit for
+bit; otherwise the attention visits the keys in another order (each shard's
+whole tiles, then one tile gathering the shards' leftover rows), which moves
+only the rounding of the key sum.
 """
 from __future__ import annotations
 
@@ -151,15 +156,12 @@ class SPStep:
         self.need_pad = self.T_pad != T
         self.fused = fused
         self.direct = direct
-        if direct:
-            if dtype != torch.bfloat16 or D not in (64, 128):
-                raise SPValueError(6, "direct: the tensor-core attention needs bf16 and D = 64 or 128")
-            if self.Tl % 128:
-                raise SPValueError(6, f"direct: token shards of {self.Tl} rows are not whole 128-row tiles")
-            if fused and self.need_pad:
-                raise SPValueError(1, f"direct + fused reads the caller's tensors in place: T={T} % W={W} != 0")
-        # shard views of the caller's tensors (direct + fused) need no buffers
+        if direct and (dtype != torch.bfloat16 or D not in (64, 128)):
+            raise SPValueError(6, "direct: the tensor-core attention needs bf16 and D = 64 or 128")
+        # shard views of the caller's tensors (direct + fused) need no buffers,
+        # no padding and no padding mask
         views = direct and fused
+        self.views = views
         names = ("k", "v") if self.cross else (("q",) if self.kv_small else ("q", "k", "v"))
         self.names = names
         emp = lambda *shape: torch.empty(*shape, dtype=dtype, device=dev)  # noqa: E731
@@ -175,13 +177,17 @@ class SPStep:
         else:
             self.out = emp(B, Tq, H, D)
             Tq_att = Tq
-        if self.kv_small or self.grid is not None:
-            self.mask = None  # every key is valid: replicated K/V, or a 2-D split with no padding
+        if self.kv_small or self.grid is not None or views:
+            # every key is valid: replicated K/V, a 2-D split with no padding,
+            # or shard views that hold no pad rows (a user mask is read as given)
+            self.mask = None
         elif mask == "key":
             self.mask = torch.empty(1, 1, self.T_pad, dtype=torch.uint8, device=dev)
         else:
             self.mask = torch.empty(B, self.T_pad, self.T_pad, dtype=torch.uint8, device=dev)
-        Tk_att = Tkv if self.kv_small else self.T_pad
+        Tk_att = Tkv if self.kv_small else (T if views else self.T_pad)
+        if views and not self.cross:
+            Tq_att = T
         self.ws_exchange = new_workspace(device=dev)
         self.ws_attn = new_workspace(sp_attention_workspace_bytes(W, B, Tq_att, Tk_att, self.Hl, D, dtype), dev)
 
@@ -196,8 +202,10 @@ class SPStep:
         return len(self.names) + (0 if self.cross else 1)
 
     def _shard_views(self, x):
-        """The W token shards of a caller tensor [B, T, H, D] as views (T % W == 0)."""
-        return [x[:, s * self.Tl:(s + 1) * self.Tl] for s in range(self.W)]
+        """The W token shards of a caller tensor [B, T, H, D] as views: shard s
+        holds tokens [s*Tl, min((s+1)*Tl, T)), the last ones short of the pad
+        rows (or empty) when T % W != 0."""
+        return [x[:, min(s * self.Tl, self.T):min((s + 1) * self.Tl, self.T)] for s in range(self.W)]
 
     def __call__(self, q, k, v, user_mask=None, timer=None, out=None):
         """Runs the step on the current stream and returns the output tensor
@@ -213,7 +221,9 @@ class SPStep:
                 for n in self.names:
                     sp_pad(src[n], self.xpad[n])
             if self.mask is None:
-                pass  # no padded keys: replicated K/V or a 2-D split
+                if self.views and self.mask_kind == "user" and user_mask is None:
+                    raise SPValueError(3, "this step was built for a user mask")
+                # no padded keys: replicated K/V, a 2-D split or in-place shard views
             elif self.mask_kind == "key":
                 sp_pad_mask(None, self.mask, self.T)
             else:
@@ -302,18 +312,22 @@ class SPStep:
                         sp_tile(self.xpad[n] if self.need_pad else src[n], self.shards[n])
             shards, o_sh = self.shards, (None if self.cross else self.o_shards)
         kind, mask = self._mask_arg()
+        if self.views and self.mask_kind == "user":
+            kind, mask = SP_MASK_FULL, user_mask  # the caller's (B, T, T) mask: no pad rows exist here
+        # the sharded operands' token count: the caller's T (in place) or the padded buffers' T_pad
+        T_sh = self.T if self.fused else self.T_pad
         with t("attention"):
             if self.kv_small:
                 kv = [(k[:, :, r * Hl:(r + 1) * Hl, :], v[:, :, r * Hl:(r + 1) * Hl, :]) for r in range(W)]
                 sp_attention_shards(shards["q"], [a for a, _ in kv], [b for _, b in kv], o_sh, self.ws_attn,
-                                    SP_SHARD_Q)
+                                    SP_SHARD_Q, Tq=T_sh)
             elif not self.cross:
                 sp_attention_shards(shards["q"], shards["k"], shards["v"], o_sh, self.ws_attn,
-                                    SP_SHARD_Q | SP_SHARD_KV, kind, mask)
+                                    SP_SHARD_Q | SP_SHARD_KV, kind, mask, Tq=T_sh, Tk=T_sh)
             else:
                 qv = [q[:, :, r * Hl:(r + 1) * Hl, :] for r in range(W)]
                 ov = [out[:, :, r * Hl:(r + 1) * Hl, :] for r in range(W)]
-                sp_attention_shards(qv, shards["k"], shards["v"], ov, self.ws_attn, SP_SHARD_KV, kind, mask)
+                sp_attention_shards(qv, shards["k"], shards["v"], ov, self.ws_attn, SP_SHARD_KV, kind, mask, Tk=T_sh)
         if not self.cross and not self.fused:
             with t("gather_output"):
                 if self.grid is not None:

@@ -272,12 +272,95 @@ def test_attention_from_shards_refuses_what_it_cannot_do():
     W, B, H, D = 4, 1, 8, 128
     ws = sp.new_workspace()
     mk = lambda Tl, dt=torch.bfloat16: [torch.zeros(B, Tl, H, D, dtype=dt, device="cuda") for _ in range(W)]  # noqa
-    with pytest.raises(ValueError):  # shards of 100 rows are not whole 128-row tiles
-        x = mk(100)
-        sp.sp_attention_shards(x, x, x, mk(100), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV)
     with pytest.raises(ValueError):  # no tensor-core kernel for fp32
         x = mk(128, torch.float32)
         sp.sp_attention_shards(x, x, x, mk(128, torch.float32), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV)
+    with pytest.raises(ValueError):  # shard 0 must hold ceil(T / W) rows
+        x = mk(100)
+        sp.sp_attention_shards(x, x, x, mk(100), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV, Tq=300, Tk=300)
+
+
+RAGGED = [
+    # W, B, T, H, D, mask_kind: shards of ceil(T / W) tokens that are not whole
+    # 128-row tiles, the last shards short (T % W != 0) or empty (T < (W-1) Tl)
+    (8, 1, 6149, 32, 128, sp.SP_MASK_NONE),   # c3 video: 769-token shards, last 764 (2 tail tiles)
+    (8, 1, 6149, 32, 128, sp.SP_MASK_KEY),    # the same with a key mask over the real tokens
+    (4, 2, 1001, 8, 64, sp.SP_MASK_FULL),     # c2 shape: 251-token shards, user mask, 4 tail tiles
+    (8, 1, 300, 16, 128, sp.SP_MASK_NONE),    # 38-token shards: no whole tile at all
+    (8, 2, 5, 8, 64, sp.SP_MASK_NONE),        # 1-token shards, shards 5..7 empty
+    (2, 1, 1000, 4, 128, sp.SP_MASK_KEY),     # 500 = 3 whole tiles + 116 per shard
+]
+
+
+@pytest.mark.parametrize("W,B,T,H,D,mask_kind", RAGGED)
+def test_attention_from_ragged_shards_matches_the_oracle(W, B, T, H, D, mask_kind):
+    # The exchange fused into the attention for any shard length: every
+    # operand is given as W views of the caller's [B, T, H, D] tensor (no
+    # padding anywhere), each rank's heads are read from every shard and O is
+    # written back in place.  Against plain attention on the unsharded tensors.
+    g = torch.Generator().manual_seed(T * 7 + W)
+    q, k, v = (torch.randn(B, T, H, D, generator=g).bfloat16().cuda() for _ in range(3))
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = (torch.rand(T, generator=g) < 0.85).to(torch.uint8)
+        mask[0] = 1
+    elif mask_kind == sp.SP_MASK_FULL:
+        mask = (torch.rand(B, T, T, generator=g) < 0.3).to(torch.uint8)
+        for b in range(B):
+            mask[b, torch.arange(T), torch.arange(T)] = 1
+    Tl = -(-T // W)
+    views = lambda x: [x[:, min(s * Tl, T):min((s + 1) * Tl, T)] for s in range(W)]  # noqa: E731
+    out = torch.full((B, T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, H // W, D, torch.bfloat16))
+    sp.sp_attention_shards(views(q), views(k), views(v), views(out), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV,
+                           mask_kind, None if mask is None else mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    got = f32_np(out)
+    assert np.isfinite(got).all()
+    m_np = None if mask is None else mask.numpy()
+    if T <= 1100:
+        ref = oracle.attention(f32_np(q), f32_np(k), f32_np(v), mask_kind, m_np)
+        assert max_abs(got, ref) <= 2e-2
+    else:
+        # every shard's first and last rows and rows in between, over every head
+        rows = []
+        for s in range(W):
+            lo, hi = s * Tl, min((s + 1) * Tl, T) - 1
+            for t in (lo, lo + 1, (lo + hi) // 2, hi - 1, hi):
+                for h in range(0, H, 5):
+                    rows.append((0, t, h))
+        rows = np.array(rows, dtype=np.int64)
+        ref = oracle.attention_rows(f32_np(q), f32_np(k), f32_np(v), rows, mask_kind, m_np)
+        assert max_abs(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= 2e-2
+
+
+@pytest.mark.parametrize("flags", [sp.SP_SHARD_KV, sp.SP_SHARD_Q])
+def test_ragged_shards_of_one_operand(flags):
+    # Only K/V (the small-query cross-attention) or only Q (a small replicated
+    # K/V) comes as ragged shards; the other operand is per rank, sliced by head.
+    W, B, H, D = 8, 1, 16, 128
+    T_sh, T_rep = 2053, 250  # sharded operand 257-token shards (last 254), replicated one 250 tokens
+    g = torch.Generator().manual_seed(flags)
+    Tq, Tk = (T_rep, T_sh) if flags == sp.SP_SHARD_KV else (T_sh, T_rep)
+    q = torch.randn(B, Tq, H, D, generator=g).bfloat16().cuda()
+    k, v = (torch.randn(B, Tk, H, D, generator=g).bfloat16().cuda() for _ in range(2))
+    mask = (torch.rand(Tk, generator=g) < 0.9).to(torch.uint8)
+    mask[0] = 1
+    Hl = H // W
+    Tl = -(-T_sh // W)
+    views = lambda x: [x[:, min(s * Tl, T_sh):min((s + 1) * Tl, T_sh)] for s in range(W)]  # noqa: E731
+    heads = lambda x: [x[:, :, r * Hl:(r + 1) * Hl] for r in range(W)]  # noqa: E731
+    out = torch.full((B, Tq, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    if flags == sp.SP_SHARD_KV:
+        sp.sp_attention_shards(heads(q), views(k), views(v), heads(out), ws, flags, sp.SP_MASK_KEY, mask.cuda())
+    else:
+        sp.sp_attention_shards(views(q), heads(k), heads(v), views(out), ws, flags, sp.SP_MASK_KEY, mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    ref = oracle.attention(f32_np(q), f32_np(k), f32_np(v), sp.SP_MASK_KEY, mask.numpy())
+    assert max_abs(f32_np(out), ref) <= 2e-2
 
 
 def test_concurrent_host_threads_give_the_same_bytes():

@@ -12,7 +12,7 @@ import torch
 import oracle
 import sequence_video_dit_gb300 as sp
 import workloads
-from gpu_helpers import f32_np, max_abs, tol_for
+from gpu_helpers import BF16_TOL, f32_np, max_abs, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -198,7 +198,7 @@ def _direct_cases():
     return [
         ("c4", c4, dict(Tq=c4.Tq), True),
         ("video6144", video, {}, True),
-        ("video6140-padded", padded, {}, False),
+        ("video6140-padded", padded, {}, True),
         ("video6144-audio1001", workloads.make_custom("a2v", W=8, B=1, T=1001, H=32, D=128, Tq=6144, index=402),
          "kv_small", True),
         ("grid16x24x16", video, dict(grid=(16, 24, 16)), False),
@@ -210,7 +210,7 @@ def _direct_cases():
 def test_direct_step_equals_staged_step_bitwise(case, fused):
     name, wl, kw, fusable = _direct_cases()[case]
     if fused and not fusable:
-        pytest.skip("in-place shards need T % W == 0 and contiguous token ranges")
+        pytest.skip("in-place shards need contiguous token ranges (the 2-D split copies)")
     inp = workloads.make_inputs(wl)
     dev = {n: inp[n].cuda() for n in ("q", "k", "v")}
     if kw == "kv_small":  # the workload's query is the sharded video, its T the audio keys
@@ -227,11 +227,37 @@ def test_direct_step_equals_staged_step_bitwise(case, fused):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
 
 
-def test_direct_step_refuses_unaligned_shards():
-    with pytest.raises(ValueError):  # c2: 1004 / 4 = 251-token shards
-        sp.SPStep(4, 2, 1001, 8, 64, mask="user", direct=True)
-    with pytest.raises(ValueError):  # padding cannot happen in place
-        sp.SPStep(8, 1, 6140, 32, 128, direct=True, fused=True)
+@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
+@pytest.mark.parametrize("fused", [False, True])
+def test_direct_step_with_ragged_shards(name, fused):
+    # Shards that are not whole 128-row tiles (c2: 251 tokens, c3: 769, c5:
+    # 6145; T % W != 0, so with fused=True the last shard view is short): the
+    # attention visits each shard's whole tiles, then one tile gathering the
+    # leftover rows.  Against the oracle (all rows of c2, sampled rows of
+    # c3 / c5 over every head) and, at tolerance, against the staged step.
+    wl = workloads.get(name)
+    inp, dev, um = _inputs(wl)
+    direct = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, direct=True, fused=fused)
+    got = direct(dev["q"], dev["k"], dev["v"], user_mask=um).clone()
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(direct.ws_attn)[0] == 0
+    assert direct.n_exchange_launches() == 0
+    got = f32_np(got)
+    assert np.isfinite(got).all()
+    q, k, v = (inp[n].float().numpy() for n in ("q", "k", "v"))
+    if name == "c2":
+        ref = oracle.attention(q, k, v, oracle.MASK_FULL, inp["user_mask"].numpy())
+        assert max_abs(got, ref) <= BF16_TOL
+    else:
+        Tl = -(-wl.T // wl.W)
+        rows = np.array([(0, t, h) for s in range(wl.W) for t in (s * Tl, min((s + 1) * Tl, wl.T) - 1)
+                         for h in (0, 13, wl.H - 1)] + [(0, wl.T - 1 - i, i) for i in range(4)], dtype=np.int64)
+        ref = oracle.attention_rows(q, k, v, rows)
+        assert max_abs(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= BF16_TOL
+    del direct
+    staged = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask)
+    ref2 = f32_np(staged(dev["q"], dev["k"], dev["v"], user_mask=um))
+    assert max_abs(got, ref2) <= BF16_TOL
 
 
 @pytest.mark.parametrize("name,kw", [("c1", {}), ("c2", {}), ("c3", {}), ("c3", dict(fused=True)),
