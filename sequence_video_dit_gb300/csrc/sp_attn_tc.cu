@@ -566,6 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int rot = nkv > 0 ? (int)(((unsigned)(qp >> 1) * 7u) % (unsigned)nkv) : 0;
     auto key_tile = [&](int jj) { int t = jj + rot; return kv0 + (t >= nkv ? t - nkv : t); };
 
+    // a split launch is followed by attn_merge_kernel, launched as its
+    // programmatic dependent: let its CTAs be scheduled once every CTA of this
+    // grid is running (they wait for this grid's completion before reading)
+    if (SPLIT && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         mbar_init(&bar_q, 1);
         for (int s = 0; s < NSLOT; s++) {
@@ -1004,8 +1008,12 @@ struct MergeParams {
     const float *part_o, *part_lse;
 };
 
+// Launched as a programmatic dependent of the attention kernel: its CTAs may
+// be scheduled while the attention grid drains, and wait here until that grid
+// has completed and its partials are visible.
 template <int NJ>
 __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // one warp per output row of a pieced work item
     const int lane = threadIdx.x & 31;
     const int64_t rowid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -1298,8 +1306,20 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         mp.part_lse = prm.part_lse;
         const int64_t rows = (int64_t)sp.n_pieced * 256;
         const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-        if (a.D == 64) tc::attn_merge_kernel<2><<<blocks, 256, 0, st>>>(mp);
-        else tc::attn_merge_kernel<4><<<blocks, 256, 0, st>>>(mp);
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(blocks, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = (a.D == 64) ? cudaLaunchKernelEx(&cfg, tc::attn_merge_kernel<2>, mp)
+                                    : cudaLaunchKernelEx(&cfg, tc::attn_merge_kernel<4>, mp);
+        if (e != cudaSuccess)
+            return set_error(SP_ERR_CUDA, "sp_attention(merge) launch failed: %s", cudaGetErrorString(e));
         return check_launch("sp_attention(merge)");
     }
     if (a.D == 64)

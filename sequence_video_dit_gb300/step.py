@@ -231,7 +231,7 @@ class SPStep:
                     raise SPValueError(3, "this step was built for a user mask")
                 sp_pad_mask(user_mask, self.mask, self.T)
         if self.direct:
-            return self._direct(q, k, v, src, out, t)
+            return self._direct(q, k, v, src, out, t, user_mask)
         if self.fused:
             with t("send_recv_heads"):
                 for n in self.names:
@@ -296,7 +296,7 @@ class SPStep:
             return SP_MASK_KEY, self.mask.view(-1)
         return SP_MASK_FULL, self.mask
 
-    def _direct(self, q, k, v, src, out, t):
+    def _direct(self, q, k, v, src, out, t, user_mask=None):
         """The step with the exchange fused into the attention: token shards in,
         O in token-shard layout out (after pad and mask, which ran already)."""
         W, Hl = self.W, self.Hl
