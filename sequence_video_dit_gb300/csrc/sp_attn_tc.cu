@@ -134,8 +134,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+// (No memory clobber: nothing in C++ reads the destination before the wait
+// below, which has one; so operands loaded before the loop stay in registers.)
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes));
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
@@ -432,17 +434,39 @@ __device__ __forceinline__ int tile_token(const Tiling &t, int W, int j, int e) 
 // apart, row e at e * 128, 16-byte chunk c at (c ^ (e & 7)) * 16), by all 32
 // lanes of the calling warp with 16-byte copies; slots that hold no token are
 // zero-filled.  base: the W shards; st: batch, token, head strides (elements).
+// Every per-shard quantity is computed once into registers (static indices
+// only), so the row loop issues its copies back to back.
 template <int D>
 __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, int tt, const uint8_t *const *base,
                                           const int64_t *st, int b, int head, int lane) {
     constexpr int CPR = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR;
+    const int64_t row_stride = st[1] * 2;
+    const int n_tail = t.tail0[W];
+    // leftover rows of shard q: tail slots [tail_q[q], ...), rows from first_q[q]
+    int tail_q[SP_MAX_RANKS];
+    const uint8_t *first_q[SP_MAX_RANKS];
+#pragma unroll
+    for (int q = 0; q < SP_MAX_RANKS; q++) {
+        const int qq = q < W ? q : W - 1;
+        tail_q[q] = q < W ? t.tail0[q] : n_tail;
+        first_q[q] = base[qq] + ((int64_t)b * st[0] + (int64_t)head * st[2]) * 2 +
+                     (int64_t)(t.full0[qq + 1] - t.full0[qq]) * 128 * row_stride + c * 16;
+    }
     for (int e = lane / CPR; e < 128; e += RPI) {
-        int s = 0, row = 0;
-        const bool ok = tiling_tail(t, W, tt * 128 + e, s, row);
-        const uint8_t *src =
-            ok ? base[s] + ((int64_t)b * st[0] + (int64_t)row * st[1] + (int64_t)head * st[2]) * 2 + c * 16 : base[0];
+        const int idx = tt * 128 + e;
+        const uint8_t *src = first_q[0];
+        int t0 = tail_q[0];
+#pragma unroll
+        for (int q = 1; q < SP_MAX_RANKS; q++) {
+            if (idx >= tail_q[q]) {
+                src = first_q[q];
+                t0 = tail_q[q];
+            }
+        }
+        const bool ok = idx < n_tail;
+        src = ok ? src + (int64_t)(idx - t0) * row_stride : first_q[0];
         const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
         cp_async_16(d, src, ok ? 16u : 0u);
     }

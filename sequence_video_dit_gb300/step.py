@@ -55,8 +55,11 @@ only the rounding of the key sum.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
+from ._lib import SP_BF16, check, lib, stream_handle
 from . import (SP_MASK_FULL, SP_MASK_KEY, SP_MASK_NONE, SP_SHARD_KV, SP_SHARD_Q, new_workspace, sp_attention_shards, sp_attention, sp_attention_workspace_bytes,
                sp_gather_2d, sp_gather_heads, sp_gather_heads_output, sp_gather_output, sp_optimal_split, sp_pad,
                sp_pad_mask, sp_pad_send_heads, sp_padded_len, sp_partition, sp_send_recv_heads, sp_tile,
@@ -230,6 +233,8 @@ class SPStep:
                 if user_mask is None:
                     raise SPValueError(3, "this step was built for a user mask")
                 sp_pad_mask(user_mask, self.mask, self.T)
+        if self.views:
+            return self._direct_inplace(q, k, v, out, t, user_mask)
         if self.direct:
             return self._direct(q, k, v, src, out, t, user_mask)
         if self.fused:
@@ -334,6 +339,58 @@ class SPStep:
                     sp_gather_2d(o_sh, out, self.grid, self.split)
                 else:
                     sp_gather_output(o_sh, out)
+        return out
+
+
+    def _direct_inplace(self, q, k, v, out, t, user_mask=None):
+        """The direct step on the caller's tensors in place (``direct=True,
+        fused=True``): one sp_attention_shards call whose shard and head-slice
+        pointers are offsets into q, k, v and out, marshalled into argument
+        arrays built once (this keeps the host cost of a short step low)."""
+        W, Hl, H, D, B, T = self.W, self.Hl, self.H, self.D, self.B, self.T
+        Tq = self.Tq if self.cross else T
+        Tk = self.Tkv if self.kv_small else T
+        want = {"q": (B, Tq, H, D), "k": (B, Tk, H, D), "v": (B, Tk, H, D), "out": (B, Tq, H, D)}
+        for name, x in (("q", q), ("k", k), ("v", v), ("out", out)):
+            if tuple(x.shape) != want[name] or x.dtype != self.dtype or not x.is_contiguous() or not x.is_cuda:
+                raise SPValueError(3, f"direct step: {name} must be a contiguous CUDA {self.dtype} {want[name]}")
+        if not hasattr(self, "_args"):
+            P = ctypes.c_void_p * W
+            self._args = [P(), P(), P(), P()]
+            self._strides = {n: (ctypes.c_int64 * 3)(sh[1] * H * D, H * D, D) for n, sh in want.items()}
+        elt, Tl = q.element_size(), self.Tl
+        qa, ka, va, oa = self._args
+
+        def shards(arr, x, n_tok):  # token shard s starts at token min(s*Tl, n_tok)
+            base = x.data_ptr()
+            for s in range(W):
+                arr[s] = base + min(s * Tl, n_tok) * H * D * elt
+
+        def heads(arr, x):  # rank r's heads of a replicated tensor, sliced in place
+            base = x.data_ptr()
+            for r in range(W):
+                arr[r] = base + r * Hl * D * elt
+
+        if self.cross:  # small query sliced per rank, K/V sharded
+            heads(qa, q), heads(oa, out), shards(ka, k, Tk), shards(va, v, Tk)
+            flags = SP_SHARD_KV
+        elif self.kv_small:  # Q sharded, small K/V sliced per rank
+            shards(qa, q, Tq), shards(oa, out, Tq), heads(ka, k), heads(va, v)
+            flags = SP_SHARD_Q
+        else:
+            shards(qa, q, T), shards(oa, out, T), shards(ka, k, T), shards(va, v, T)
+            flags = SP_SHARD_Q | SP_SHARD_KV
+        kind, mptr = SP_MASK_NONE, None
+        if self.mask_kind == "user" and not self.cross and not self.kv_small:
+            if user_mask is None or tuple(user_mask.shape) != (B, T, T) or user_mask.element_size() != 1 \
+                    or not user_mask.is_contiguous() or not user_mask.is_cuda:
+                raise SPValueError(3, f"direct step: the user mask must be a contiguous uint8 CUDA ({B}, {T}, {T})")
+            kind, mptr = SP_MASK_FULL, user_mask.data_ptr()
+        ws = self.ws_attn
+        with t("attention"):
+            check(lib().sp_attention_shards(qa, ka, va, oa, W, B, Tq, Tk, H, D, SP_BF16, flags, self._strides["q"],
+                                            self._strides["k"], self._strides["out"], kind, mptr, 0.0,
+                                            ws.data_ptr(), ws.numel() * ws.element_size(), stream_handle(None)))
         return out
 
 
