@@ -434,8 +434,8 @@ __device__ __forceinline__ int tile_token(const Tiling &t, int W, int j, int e) 
 // apart, row e at e * 128, 16-byte chunk c at (c ^ (e & 7)) * 16), by all 32
 // lanes of the calling warp with 16-byte copies; slots that hold no token are
 // zero-filled.  base: the W shards; st: batch, token, head strides (elements).
-// Every per-shard quantity is computed once into registers (static indices
-// only), so the row loop issues its copies back to back.
+// Each lane walks its rows (every RPI-th slot) with a running source pointer
+// and recomputes it only where the walk crosses into the next shard.
 template <int D>
 __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, int tt, const uint8_t *const *base,
                                           const int64_t *st, int b, int head, int lane) {
@@ -443,32 +443,23 @@ __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, 
     constexpr int RPI = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR;
     const int64_t row_stride = st[1] * 2;
+    const int64_t off = ((int64_t)b * st[0] + (int64_t)head * st[2]) * 2 + c * 16;
     const int n_tail = t.tail0[W];
-    // leftover rows of shard q: tail slots [tail_q[q], ...), rows from first_q[q]
-    int tail_q[SP_MAX_RANKS];
-    const uint8_t *first_q[SP_MAX_RANKS];
-#pragma unroll
-    for (int q = 0; q < SP_MAX_RANKS; q++) {
-        const int qq = q < W ? q : W - 1;
-        tail_q[q] = q < W ? t.tail0[q] : n_tail;
-        first_q[q] = base[qq] + ((int64_t)b * st[0] + (int64_t)head * st[2]) * 2 +
-                     (int64_t)(t.full0[qq + 1] - t.full0[qq]) * 128 * row_stride + c * 16;
-    }
-    for (int e = lane / CPR; e < 128; e += RPI) {
-        const int idx = tt * 128 + e;
-        const uint8_t *src = first_q[0];
-        int t0 = tail_q[0];
-#pragma unroll
-        for (int q = 1; q < SP_MAX_RANKS; q++) {
-            if (idx >= tail_q[q]) {
-                src = first_q[q];
-                t0 = tail_q[q];
-            }
+    const uint8_t *const zsrc = base[0];  // any valid address: zero-filled copies read nothing
+    int e = lane / CPR, idx = tt * 128 + e;
+    int s = 0;
+    while (s + 1 < W && idx >= t.tail0[s + 1]) s++;
+    int end = t.tail0[s + 1];
+    const uint8_t *src = base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
+    for (; e < 128; e += RPI, idx += RPI, src += RPI * row_stride) {
+        while (idx >= end && s + 1 < W) {
+            s++;
+            end = t.tail0[s + 1];
+            src = base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
         }
         const bool ok = idx < n_tail;
-        src = ok ? src + (int64_t)(idx - t0) * row_stride : first_q[0];
         const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
-        cp_async_16(d, src, ok ? 16u : 0u);
+        cp_async_16(d, ok ? src : zsrc, ok ? 16u : 0u);
     }
     cp_async_wait_all();
     fence_proxy_async_smem();  // the tensor core (async proxy) reads what these copies wrote
