@@ -139,10 +139,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// Waits until at most 2 of this thread's copy groups are still in flight.
-__device__ __forceinline__ void cp_async_wait_2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -462,13 +461,8 @@ __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, 
         const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
         cp_async_16(d, ok ? src : zsrc, ok ? 16u : 0u);
     }
-    cp_async_commit();
-}
-// Completes every tail fill this thread has issued: its copies have landed and
-// are ordered before the tensor core's (async-proxy) reads of them.
-__device__ __forceinline__ void fill_tail_complete() {
     cp_async_wait_all();
-    fence_proxy_async_smem();
+    fence_proxy_async_smem();  // the tensor core (async proxy) reads what these copies wrote
 }
 
 // Visibility bits of tail key tile tt for this thread's query row (global
@@ -683,35 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (!qwhole[i])
                     fill_tail<D>(sbase + C::Q_OFF + i * C::TILE, p.qtl, p.W, 2 * qp + i - p.qtl.full0[p.W], p.qptr,
                                  p.qs, b, qhead[i], lane);
-            if (!qwhole[0] || !qwhole[1]) fill_tail_complete();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_q);
             const int stall = *p.kv_stall;  // 0 in normal use
             const int nloads = stall > 0 ? min(2 * nkv, stall - 1) : 2 * nkv;
-            // Tail fills are announced late so that their copies fly while the
-            // producer goes on: one copy group per fill, at most the two newest
-            // unannounced after a fill, none after a TMA load.  The MMA thread's
-            // release of the slot a wait needs (load n - NSLOT) depends on loads up
-            // to n - NSLOT + 1 only, so the unannounced ones (n - 2, n - 1) never
-            // block it.
-            int pend[3], npend = 0;  // slots of unannounced fills, oldest first
-            auto announce = [&](bool all) {
-                if (npend == 0) return;
-                int done = npend;
-                if (all) {
-                    cp_async_wait_all();
-                } else {
-                    cp_async_wait_2();
-                    done = npend - 2;
-                    if (done <= 0) return;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    for (int q = 0; q < done; q++) mbar_arrive(&bar_full[pend[q]]);
-                for (int q = done; q < npend; q++) pend[q - done] = pend[q];
-                npend -= done;
-            };
             int n = 0;
             for (; n < nloads; n++) {
                 const int slot = n % NSLOT;
@@ -730,15 +699,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                             tma_load_4d(&bar_full[slot], m, sbase + C::R_OFF + slot * C::TILE + db * 16384, db * 64,
                                         khead, krow, b);
                     }
-                    announce(true);
                 } else {
                     fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.full0[p.W],
                                  (n & 1) ? p.vptr : p.kptr, p.ks, b, khead, lane);
-                    pend[npend++] = slot;
-                    announce(false);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_full[slot]);
                 }
             }
-            announce(true);  // (also after an abort: the copies land before the CTA exits)
             if (lane == 0) {
                 wait_drain(&bar_q, 0);
                 for (int slot = 0; slot < NSLOT && slot < n; slot++) {
