@@ -331,21 +331,23 @@ def run_ours(args, world, rank, local):
     x_bytes = step.exchange_bytes_per_launch() * step.n_exchange_launches() * args.steps
     exch_gbs = x_bytes / (x_ms / 1e3) / 1e9 if x_ms > 0 else None
 
+    # ---- end to end, right after the device-resident steps (same state of the
+    # GPU): pinned host inputs copied in and the output copied out every step,
+    # inside the timed region.  Uploads and downloads run on two copy streams,
+    # so step i+1's uploads and step i-1's download overlap step i's compute
+    # (two input and two output buffers, ordered by events), as a streaming
+    # user of the library would run it.
+    h2d = in_bytes + (um_host.numel() if um_host is not None else 0)
+    d2h = out_host.numel() * out_host.element_size()
+    with ClockSampler(dev.index) as clk_e2e:
+        e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev)
+    link = measure_link(host, out_host, dev)
     # ---- the same step through the fused exchange entry points (pad + tile +
     # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
     fused = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush)
     direct = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=True) \
         if direct_eligible(wl, world) else None
     graphed = time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush)
-    # ---- end to end: pinned host inputs copied in and the output copied out
-    # every step, inside the timed region.  Copies run on their own stream so
-    # step i+1's uploads and step i's download overlap step i's compute (two
-    # input and two output buffers, ordered by events), as a streaming user
-    # of the library would run it.
-    h2d = in_bytes + (um_host.numel() if um_host is not None else 0)
-    d2h = out_host.numel() * out_host.element_size()
-    e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev)
-    link = measure_link(host, out_host, dev)
     # lower bound of a pipelined end-to-end step: the slower of the device
     # step and the step's copies over the link (both directions at once)
     e2e_bound_ms = max(ms, link["both_directions_ms"])
@@ -379,7 +381,7 @@ def run_ours(args, world, rank, local):
                 "copies": "pinned host buffers on two copy streams; H2D of step i+1 and D2H of step i-1 overlap "
                           "step i's compute",
                 "link": link, "bound_ms_per_step": round(e2e_bound_ms, 4),
-                "frac_of_bound": round(e2e_bound_ms / e2e_ms, 4)},
+                "frac_of_bound": round(e2e_bound_ms / e2e_ms, 4), "clocks": clk_e2e.summary()},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,

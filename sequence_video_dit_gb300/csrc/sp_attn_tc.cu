@@ -71,16 +71,26 @@ struct Cfg {
 // How the 128-row tiles of one operand map onto its memory.  A per-rank
 // tensor (sharded == 0): tile j is rows [128 j, 128 j + 128).  W source token
 // shards (sharded != 0): global token g lives in shard g / Tl at row g % Tl,
-// and shard s holds n_s real rows.  The tiles are every shard's whole
-// 128-row tiles in shard order (shard s owns tiles [full0[s], full0[s+1])),
-// then "tail" tiles that gather the rows each shard has left after its whole
-// tiles, n_s % 128 of them, in shard order (shard s's leftovers are tail
-// slots [tail0[s], tail0[s+1])); slots past tail0[W] hold no token.  With
-// Tl a multiple of 128 and every shard full there are no tail tiles and tile j
-// is global rows [128 j, 128 j + 128), the order of the exchanged layout.
+// and shard s holds rows[s] real rows.  The tiles are, in this order:
+//   - every shard's whole 128-row tiles, in shard order (shard s owns tiles
+//     [full0[s], full0[s+1]));
+//   - "partial" tiles: one per shard whose leftover block (rows[s] % 128
+//     rows after its whole tiles) holds at least kPartialMin rows, loaded by
+//     TMA from the shard like a whole tile, the rows past the shard's end
+//     reading as zeros and masked off (shards part[0 .. npart));
+//   - "gathered" tiles from tile g0 = full0[W] + npart on: the smaller
+//     leftover blocks, packed in shard order (shard s's are gathered slots
+//     [tail0[s], tail0[s+1])) and copied row by row; slots past tail0[W]
+//     hold no token.
+// With Tl a multiple of 128 (and only the last shard short) the tiles are
+// exactly global rows [128 j, 128 j + 128), the order of the exchanged layout.
+constexpr int kPartialMin = 64;
 struct Tiling {
     int sharded;
     int Tl;
+    int npart, g0;
+    int rows[SP_MAX_RANKS];
+    int part[SP_MAX_RANKS];
     int full0[SP_MAX_RANKS + 1];
     int tail0[SP_MAX_RANKS + 1];
 };
@@ -132,6 +142,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void st_shared_zero16(uint32_t dst) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u));
 }
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 // (No memory clobber: nothing in C++ reads the destination before the wait
@@ -385,18 +398,26 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
     }
 }
 
-// Whole tile j of a sharded operand: its shard s and first row; false when j
-// is a tail tile (or past the last tile).
-__device__ __forceinline__ bool tiling_whole(const Tiling &t, int W, int j, int &s, int &row) {
-    if (j >= t.full0[W]) return false;
-    int q = 0;
-    while (q + 1 < W && j >= t.full0[q + 1]) q++;
-    s = q;
-    row = (j - t.full0[q]) * 128;
+// Tile j of a sharded operand when TMA loads it (a whole or a partial tile):
+// its shard s, first row and the number of its rows that hold tokens; false
+// for a gathered tile (or past the last tile).
+__device__ __forceinline__ bool tiling_box(const Tiling &t, int W, int j, int &s, int &row, int &nvalid) {
+    if (j < t.full0[W]) {
+        int q = 0;
+        while (q + 1 < W && j >= t.full0[q + 1]) q++;
+        s = q;
+        row = (j - t.full0[q]) * 128;
+        nvalid = 128;
+        return true;
+    }
+    const int k = j - t.full0[W];
+    if (k >= t.npart) return false;
+    s = t.part[k];
+    row = (t.full0[s + 1] - t.full0[s]) * 128;
+    nvalid = t.rows[s] - row;
     return true;
 }
-// Tail slot idx (counted over every shard's leftover rows): its shard s and
-// row; false past the last leftover row.
+// Gathered slot idx: its shard s and row; false past the last gathered row.
 __device__ __forceinline__ bool tiling_tail(const Tiling &t, int W, int idx, int &s, int &row) {
     if (idx < 0 || idx >= t.tail0[W]) return false;
     int q = 0;
@@ -407,8 +428,8 @@ __device__ __forceinline__ bool tiling_tail(const Tiling &t, int W, int idx, int
 }
 // Where tile j of rank r's local head h comes from when TMA can load it:
 // the rank's own tensor (map r, head h, rows [128 j, 128 j + 128)) or a
-// whole tile of source shard s (map s, head r * Hl + h).  False for a tail
-// tile, which the producer warp assembles row by row.
+// whole or partial tile of source shard s (map s, head r * Hl + h).  False
+// for a gathered tile, which the producer warp assembles row by row.
 __device__ __forceinline__ bool tile_src(const Tiling &t, int W, int j, int r, int h, int Hl, int &map, int &head,
                                          int &row) {
     if (!t.sharded) {
@@ -418,14 +439,15 @@ __device__ __forceinline__ bool tile_src(const Tiling &t, int W, int j, int r, i
         return true;
     }
     head = r * Hl + h;
-    return tiling_whole(t, W, j, map, row);
+    int nvalid;
+    return tiling_box(t, W, j, map, row, nvalid);
 }
-// Global token of row e of tile j, or -1 when the slot holds no token.
+// Global token of row e of tile j, or -1 when the slot holds none.
 __device__ __forceinline__ int tile_token(const Tiling &t, int W, int j, int e) {
     if (!t.sharded) return j * 128 + e;
-    int s, row;
-    if (tiling_whole(t, W, j, s, row)) return s * t.Tl + row + e;
-    if (tiling_tail(t, W, (j - t.full0[W]) * 128 + e, s, row)) return s * t.Tl + row;
+    int s, row, nvalid;
+    if (tiling_box(t, W, j, s, row, nvalid)) return e < nvalid ? s * t.Tl + row + e : -1;
+    if (tiling_tail(t, W, (j - t.g0) * 128 + e, s, row)) return s * t.Tl + row;
     return -1;
 }
 
@@ -445,7 +467,6 @@ __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, 
     const int64_t row_stride = st[1] * 2;
     const int64_t off = ((int64_t)b * st[0] + (int64_t)head * st[2]) * 2 + c * 16;
     const int n_tail = t.tail0[W];
-    const uint8_t *const zsrc = base[0];  // any valid address: zero-filled copies read nothing
     int e = lane / CPR, idx = tt * 128 + e;
     int s = 0;
     while (s + 1 < W && idx >= t.tail0[s + 1]) s++;
@@ -457,9 +478,9 @@ __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, 
             end = t.tail0[s + 1];
             src = base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
         }
-        const bool ok = idx < n_tail;
         const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
-        cp_async_16(d, ok ? src : zsrc, ok ? 16u : 0u);
+        if (idx < n_tail) cp_async_16(d, src, 16u);
+        else st_shared_zero16(d);  // no token: zeros (an empty V row must not hold stale non-finite bits)
     }
     cp_async_wait_all();
     fence_proxy_async_smem();  // the tensor core (async proxy) reads what these copies wrote
@@ -509,12 +530,20 @@ __device__ __forceinline__ void tail_words(const TcParams &p, int b, int q_row, 
 // Visibility bits of key tile j (any tiling) for this thread's query row.
 __device__ __forceinline__ void key_words(const TcParams &p, int b, int q_row, int j, int lane, uint32_t w[4]) {
     int s, row;
+    int nvalid;
     if (!p.ktl.sharded) {
         mask_words(p, b, q_row, j * 128, lane, w);
-    } else if (tiling_whole(p.ktl, p.W, j, s, row)) {
-        mask_words(p, b, q_row, s * p.ktl.Tl + row, lane, w);  // 128 consecutive real tokens
+    } else if (tiling_box(p.ktl, p.W, j, s, row, nvalid)) {
+        mask_words(p, b, q_row, s * p.ktl.Tl + row, lane, w);  // consecutive tokens of shard s
+        if (nvalid < 128) {  // a partial tile: its rows past the shard's end hold no key
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const int n = nvalid - 32 * g;
+                w[g] &= n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+            }
+        }
     } else {
-        tail_words(p, b, q_row, j - p.ktl.full0[p.W], lane, w);
+        tail_words(p, b, q_row, j - p.ktl.g0, lane, w);
     }
 }
 
@@ -675,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             for (int i = 0; i < 2; i++)
                 if (!qwhole[i])
-                    fill_tail<D>(sbase + C::Q_OFF + i * C::TILE, p.qtl, p.W, 2 * qp + i - p.qtl.full0[p.W], p.qptr,
+                    fill_tail<D>(sbase + C::Q_OFF + i * C::TILE, p.qtl, p.W, 2 * qp + i - p.qtl.g0, p.qptr,
                                  p.qs, b, qhead[i], lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_q);
@@ -700,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                         khead, krow, b);
                     }
                 } else {
-                    fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.full0[p.W],
+                    fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.g0,
                                  (n & 1) ? p.vptr : p.kptr, p.ks, b, khead, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar_full[slot]);
@@ -961,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     // tail query tile: every thread stores its own row, if it holds a token
                     int s = 0, srow = 0;
                     const bool mine =
-                        q_row < p.Tq && tiling_tail(p.qtl, p.W, (2 * qp + i - p.qtl.full0[p.W]) * 128 + row, s, srow);
+                        q_row < p.Tq && tiling_tail(p.qtl, p.W, (2 * qp + i - p.qtl.g0) * 128 + row, s, srow);
                     uint8_t *orow_ptr = mine ? p.optr[s] + ((int64_t)b * p.os[0] + (int64_t)srow * p.os[1] +
                                                             (int64_t)(r * p.Hl + h) * p.os[2]) * 2
                                              : nullptr;
@@ -1048,9 +1077,11 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(MergeParams a) {
     } else {
         const int j = qp * 2 + (row >> 7), e = row & 127;
         int s, srow;
-        if (tiling_whole(a.qtl, a.W, j, s, srow)) {
+        int nvalid;
+        if (tiling_box(a.qtl, a.W, j, s, srow, nvalid)) {
+            if (e >= nvalid) return;  // past the end of a partial tile: no query
             srow += e;
-        } else if (!tiling_tail(a.qtl, a.W, (j - a.qtl.full0[a.W]) * 128 + e, s, srow)) {
+        } else if (!tiling_tail(a.qtl, a.W, (j - a.qtl.g0) * 128 + e, s, srow)) {
             return;  // the slot holds no query
         }
         omap = s;
@@ -1122,10 +1153,14 @@ static void make_tiling(Tiling &t, int Tl, int T, int W) {
     t.sharded = 1;
     t.Tl = Tl;
     for (int s = 0; s < W; s++) {
-        const int n = map_rows(Tl, T, s);
+        const int n = map_rows(Tl, T, s), rem = n % 128;
+        const bool partial = rem >= kPartialMin;
+        t.rows[s] = n;
+        if (partial) t.part[t.npart++] = s;
         t.full0[s + 1] = t.full0[s] + n / 128;
-        t.tail0[s + 1] = t.tail0[s] + n % 128;
+        t.tail0[s + 1] = t.tail0[s] + (partial ? 0 : rem);
     }
+    t.g0 = t.full0[W] + t.npart;
 }
 
 // Work decomposition.  A work item is one (rank, batch, head, query pair); a
