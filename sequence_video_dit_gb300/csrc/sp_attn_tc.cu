@@ -533,6 +533,8 @@ __device__ __forceinline__ void key_words(const TcParams &p, int b, int q_row, i
     int nvalid;
     if (!p.ktl.sharded) {
         mask_words(p, b, q_row, j * 128, lane, w);
+    } else if (p.mask_kind == SP_MASK_NONE && j < p.ktl.full0[p.W]) {
+        w[0] = w[1] = w[2] = w[3] = 0xffffffffu;  // a whole tile of real keys
     } else if (tiling_box(p.ktl, p.W, j, s, row, nvalid)) {
         mask_words(p, b, q_row, s * p.ktl.Tl + row, lane, w);  // consecutive tokens of shard s
         if (nvalid < 128) {  // a partial tile: its rows past the shard's end hold no key
@@ -719,9 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     ok = wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
                 const int j = key_tile(n >> 1);
-                int kmap, khead, krow;
-                if (tile_src(p.ktl, p.W, j, r, h, p.Hl, kmap, khead, krow)) {
-                    if (lane == 0) {
+                if (!p.ktl.sharded || j < p.ktl.g0) {
+                    if (lane == 0) {  // a TMA tile: lane 0 alone
+                        int kmap, khead, krow;
+                        tile_src(p.ktl, p.W, j, r, h, p.Hl, kmap, khead, krow);
                         mbar_arrive_expect_tx(&bar_full[slot], SLOT);
                         const CUtensorMap *m = (n & 1) ? &p.tv[kmap] : &p.tk[kmap];
                         for (int db = 0; db < C::DB; db++)
@@ -730,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     }
                 } else {
                     fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.g0,
-                                 (n & 1) ? p.vptr : p.kptr, p.ks, b, khead, lane);
+                                 (n & 1) ? p.vptr : p.kptr, p.ks, b, r * p.Hl + h, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar_full[slot]);
                 }
