@@ -379,7 +379,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(weak_scaling_value(flops, world, e2e_ms / 1e3), 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "copies": "pinned host buffers on two copy streams; H2D of step i+1 and D2H of step i-1 overlap "
-                          "step i's compute",
+                          "step i's compute (the step replayed from a CUDA graph per buffer set)",
                 "link": link, "bound_ms_per_step": round(e2e_bound_ms, 4),
                 "frac_of_bound": round(e2e_bound_ms / e2e_ms, 4), "clocks": clk_e2e.summary()},
         "gpu_launches": launches,
@@ -474,10 +474,11 @@ def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> 
 
 def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev) -> float:
     """Mean ms per step of `steps` end-to-end steps (H2D of every step's inputs,
-    the step, D2H of its output).  Uploads and downloads run on two copy
-    streams of their own, so step i+1's uploads, step i's compute and step
-    i-1's download can all be in flight at once (two input and two output
-    buffers, ordered by events)."""
+    the step, D2H of its output).  Two input and two output buffer sets, each
+    with the step captured once as a CUDA graph (SPStep.capture), so the host
+    issues one replay per step.  Uploads and downloads run on two copy streams
+    of their own: step i+1's uploads, step i's compute and step i-1's download
+    can all be in flight at once (ordered by events)."""
     main = torch.cuda.current_stream(dev)
     up = torch.cuda.Stream(device=dev)
     down = torch.cuda.Stream(device=dev)
@@ -485,6 +486,11 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
     d_um = [um_host.to(dev) if um_host is not None else None for _ in range(2)]
     d_out = [torch.empty_like(step.out) for _ in range(2)]
     out_pin = [out_host, torch.empty_like(out_host).pin_memory()]
+    for b in range(2):
+        for n in host:
+            d_in[b][n].copy_(host[n])
+    graphs = [step.capture(d_in[b]["q"], d_in[b]["k"], d_in[b]["v"], user_mask=d_um[b], out=d_out[b])
+              for b in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
     ev_d2h = [torch.cuda.Event() for _ in range(2)]
@@ -514,7 +520,7 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
         main.wait_event(ev_in[b])
         if i >= 2:
             main.wait_event(ev_d2h[b])  # step i-2's output has left d_out[b]
-        step(d_in[b]["q"], d_in[b]["k"], d_in[b]["v"], user_mask=d_um[b], out=d_out[b])
+        graphs[b].replay()
         ev_done[b].record(main)
         down.wait_event(ev_done[b])
         with torch.cuda.stream(down):
@@ -525,6 +531,7 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
     t1.record(main)
     torch.cuda.synchronize()
     barrier(world)
+    del graphs
     return max_over_ranks(t0.elapsed_time(t1) / steps, world)
 
 

@@ -34,9 +34,9 @@
 // pieces' fp32 partials are merged by LSE in attn_merge_kernel.
 // Operands are either each rank's tensors or, for the exchange fused into
 // the attention, the source ranks' token shards (Tiling): every shard's whole
-// 128-row tiles come by TMA from the shard, and the rows the shards have
-// left over are gathered into tail tiles that the producer warp copies row
-// by row into the same swizzled layout.
+// 128-row tiles, and its leftover block when that holds at least half a tile,
+// come by TMA from the shard; smaller leftover blocks are gathered into tiles
+// that the producer warp copies row by row into the same swizzled layout.
 //
 // Every mbarrier wait is bounded (%globaltimer); on timeout the CTA records
 // SP_ERR_TIMEOUT, every role stops, in-flight copies and MMAs are drained
