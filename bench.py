@@ -653,6 +653,9 @@ def run_profile(args):
     import sequence_video_dit_gb300 as sp
 
     wl = workloads.get(args.workload)
+    if args.tokens:  # the workload's shape with a shorter sequence (a small case for long captures)
+        wl = workloads.make_custom(f"{wl.name}-T{args.tokens}", W=wl.W, B=wl.B, T=args.tokens, H=wl.H, D=wl.D,
+                                   dtype=wl.dtype, mask=wl.mask, Tq=wl.Tq, input_scale=wl.input_scale, index=wl.index)
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = workloads.make_inputs(wl)
     d_in = {n: inp[n].to(dev) for n in ("q", "k", "v")}
@@ -677,6 +680,8 @@ def main():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--profile", choices=["staged", "fused", "direct"],
                     help="run --steps steps of this step variant untimed (a target for ncu) and exit")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="with --profile: the workload's shape with this sequence length instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
