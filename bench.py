@@ -655,7 +655,8 @@ def run_profile(args):
     wl = workloads.get(args.workload)
     if args.tokens:  # the workload's shape with a shorter sequence (a small case for long captures)
         wl = workloads.make_custom(f"{wl.name}-T{args.tokens}", W=wl.W, B=wl.B, T=args.tokens, H=wl.H, D=wl.D,
-                                   dtype=wl.dtype, mask=wl.mask, Tq=wl.Tq, input_scale=wl.input_scale, index=wl.index)
+                                   dtype=wl.dtype, mask=wl.mask, Tq=wl.Tq, input_scale=wl.input_scale,
+                                   index=wl.index)
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = workloads.make_inputs(wl)
     d_in = {n: inp[n].to(dev) for n in ("q", "k", "v")}
