@@ -451,37 +451,47 @@ __device__ __forceinline__ int tile_token(const Tiling &t, int W, int j, int e) 
     return -1;
 }
 
-// Tail tile tt of a sharded operand into the 128-byte-swizzled tile at
+// Gathered tile tt of a sharded operand into the 128-byte-swizzled tile at
 // shared address dst (the layout a TMA box writes: 64-column blocks 16 KB
 // apart, row e at e * 128, 16-byte chunk c at (c ^ (e & 7)) * 16), by all 32
-// lanes of the calling warp with 16-byte copies; slots that hold no token are
-// zero-filled.  base: the W shards; st: batch, token, head strides (elements).
-// Each lane walks its rows (every RPI-th slot) with a running source pointer
-// and recomputes it only where the walk crosses into the next shard.
+// lanes of the calling warp with 16-byte copies.  base: the W shards; st:
+// batch, token, head strides (elements).  Each lane walks its rows (every
+// RPI-th slot) with a running source pointer, recomputed only where the walk
+// crosses into the next shard.  Slots past the last gathered row are left as
+// they are, or zeroed when zero_empty: an empty K row is masked whatever it
+// holds, and an empty Q row yields an output row that is never stored, but an
+// empty V row is multiplied by P = 0 and must not hold non-finite bits, which
+// only a slot this CTA has not filled before can.
 template <int D>
 __device__ __forceinline__ void fill_tail(uint32_t dst, const Tiling &t, int W, int tt, const uint8_t *const *base,
-                                          const int64_t *st, int b, int head, int lane) {
+                                          const int64_t *st, int b, int head, int lane, bool zero_empty) {
     constexpr int CPR = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;  // rows per pass of the warp
     const int c = lane % CPR;
     const int64_t row_stride = st[1] * 2;
     const int64_t off = ((int64_t)b * st[0] + (int64_t)head * st[2]) * 2 + c * 16;
-    const int n_tail = t.tail0[W];
+    const int nvalid = min(max(t.tail0[W] - tt * 128, 0), 128);
     int e = lane / CPR, idx = tt * 128 + e;
-    int s = 0;
-    while (s + 1 < W && idx >= t.tail0[s + 1]) s++;
-    int end = t.tail0[s + 1];
-    const uint8_t *src = base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
-    for (; e < 128; e += RPI, idx += RPI, src += RPI * row_stride) {
-        while (idx >= end && s + 1 < W) {
-            s++;
-            end = t.tail0[s + 1];
-            src = base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
+    if (e < nvalid) {
+        int s = 0;
+        while (s + 1 < W && idx >= t.tail0[s + 1]) s++;
+        int end = t.tail0[s + 1];
+        const uint8_t *src =
+            base[s] + off + ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
+        for (; e < nvalid; e += RPI, idx += RPI, src += RPI * row_stride) {
+            while (idx >= end && s + 1 < W) {
+                s++;
+                end = t.tail0[s + 1];
+                src = base[s] + off +
+                      ((int64_t)(t.full0[s + 1] - t.full0[s]) * 128 + (idx - t.tail0[s])) * row_stride;
+            }
+            const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
+            cp_async_16(d, src, 16u);
         }
-        const uint32_t d = dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4));
-        if (idx < n_tail) cp_async_16(d, src, 16u);
-        else st_shared_zero16(d);  // no token: zeros (an empty V row must not hold stale non-finite bits)
     }
+    if (zero_empty)
+        for (; e < 128; e += RPI)
+            st_shared_zero16(dst + (uint32_t)((c >> 3) * 16384 + e * 128 + (((c & 7) ^ (e & 7)) << 4)));
     cp_async_wait_all();
     fence_proxy_async_smem();  // the tensor core (async proxy) reads what these copies wrote
 }
@@ -707,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (int i = 0; i < 2; i++)
                 if (!qwhole[i])
                     fill_tail<D>(sbase + C::Q_OFF + i * C::TILE, p.qtl, p.W, 2 * qp + i - p.qtl.g0, p.qptr,
-                                 p.qs, b, qhead[i], lane);
+                                 p.qs, b, qhead[i], lane, false);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_q);
             const int stall = *p.kv_stall;  // 0 in normal use
@@ -732,8 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                         khead, krow, b);
                     }
                 } else {
+                    // a V slot this CTA has not filled yet gets its empty rows zeroed
                     fill_tail<D>(sbase + C::R_OFF + slot * C::TILE, p.ktl, p.W, j - p.ktl.g0,
-                                 (n & 1) ? p.vptr : p.kptr, p.ks, b, r * p.Hl + h, lane);
+                                 (n & 1) ? p.vptr : p.kptr, p.ks, b, r * p.Hl + h, lane, (n & 1) && use == 0);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar_full[slot]);
                 }
