@@ -344,9 +344,8 @@ def run_ours(args, world, rank, local):
     link = measure_link(host, out_host, dev)
     # ---- the same step through the fused exchange entry points (pad + tile +
     # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
-    fused = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush)
-    direct = time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=True) \
-        if direct_eligible(wl, world) else None
+    fused, direct = time_variants(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush,
+                                  with_direct=direct_eligible(wl, world))
     graphed = time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush)
     # lower bound of the pipelined end-to-end step: the slower of the device
     # step (eager or graph-replayed, whichever is faster: the end-to-end loop
@@ -406,42 +405,52 @@ def direct_eligible(wl, world=1) -> bool:
     return wl.dtype == "bf16" and wl.D in (64, 128)
 
 
-def time_fused_step(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, direct=False) -> dict:
-    """Device-resident timing of the step built with ``fused=True`` (and with
-    ``direct=True``: the exchange fused into the attention, in place), same
-    inputs and the same output bits, reported beside the staged step."""
+def time_variants(wl, d_in, d_um, dev, args, world, flops, big_inputs, flush, with_direct=True):
+    """Device-resident timing of the step built with ``fused=True`` and of the
+    one with ``direct=True, fused=True`` (the exchange inside the attention, in
+    place), on the same inputs.  Their steps alternate inside one timed loop,
+    so a slow drift of the clocks over the run affects both alike."""
     import sequence_video_dit_gb300 as sp
     from sequence_video_dit_gb300.step import StageTimer
 
-    step = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq, device=dev,
-                     fused=True, direct=direct)
+    steps = {"fused": sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq,
+                                device=dev, fused=True)}
+    if with_direct:
+        steps["direct"] = sp.SPStep(wl.W, wl.B, wl.T, wl.H, wl.D, dtype=wl.torch_dtype, mask=wl.mask, Tq=wl.Tq,
+                                    device=dev, fused=True, direct=True)
     for _ in range(args.warmup):
-        step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
-    timer = StageTimer()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    n0 = sp.lib().sp_launch_count()
+        for st in steps.values():
+            st(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um)
+    timers = {n: StageTimer() for n in steps}
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for n in steps}
+    launches = {n: 0 for n in steps}
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        if not big_inputs:
-            flush.zero_()
-        starts[i].record()
-        step(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um, timer=timer)
-        ends[i].record()
+        for n, st in steps.items():
+            if not big_inputs:
+                flush.zero_()
+            n0 = sp.lib().sp_launch_count()
+            ev[n][i][0].record()
+            st(d_in["q"], d_in["k"], d_in["v"], user_mask=d_um, timer=timers[n])
+            ev[n][i][1].record()
+            launches[n] += int(sp.lib().sp_launch_count() - n0)
     torch.cuda.synchronize()
     barrier(world)
-    launches = int(sp.lib().sp_launch_count() - n0)
-    st = sp.sp_workspace_status(step.ws_exchange)[0] | sp.sp_workspace_status(step.ws_attn)[0]
-    if st != 0:
-        raise RuntimeError(f"device status {st} after the fused step")
-    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps, world)
-    tot, cnt = timer.totals_ms(), timer.counts()
-    out = {"value": round(weak_scaling_value(flops, world, ms / 1e3), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
-           "stage_ms": {k: round(v / cnt[k], 4) for k, v in tot.items()}, "gpu_launches": launches}
-    del step
+    out = {}
+    for n, st in steps.items():
+        code = sp.sp_workspace_status(st.ws_exchange)[0] | sp.sp_workspace_status(st.ws_attn)[0]
+        if code != 0:
+            raise RuntimeError(f"device status {code} after the {n} step")
+        ms = max_over_ranks(sum(a.elapsed_time(z) for a, z in ev[n]) / args.steps, world)
+        tot, cnt = timers[n].totals_ms(), timers[n].counts()
+        out[n] = {"value": round(weak_scaling_value(flops, world, ms / 1e3), 3), "unit": UNIT,
+                  "ms_per_step": round(ms, 4), "stage_ms": {k: round(v / cnt[k], 4) for k, v in tot.items()},
+                  "gpu_launches": launches[n]}
+    del steps
     torch.cuda.empty_cache()
-    return out
+    return out["fused"], out.get("direct")
 
 
 def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> dict:
