@@ -345,6 +345,30 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_pack_u(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -353,14 +377,31 @@ __device__ __forceinline__ uint32_t nibble_of(uint32_t v) {
     return ((v & 0x000000ffu) ? 1u : 0u) | ((v & 0x0000ff00u) ? 2u : 0u) | ((v & 0x00ff0000u) ? 4u : 0u) |
            ((v & 0xff000000u) ? 8u : 0u);
 }
-// Visibility bits of keys [k, k+4) of one mask row (bounds-checked).
-__device__ __forceinline__ uint32_t mask_nibble(const uint8_t *row, int k, int Tk, bool vec4) {
-    if (vec4 && k + 3 < Tk) return nibble_of(*reinterpret_cast<const uint32_t *>(row + k));
-    uint32_t n = 0;
+// Mask bytes of keys [k, k+4) of one mask row, as one word (bounds-checked:
+// a key past Tk reads as masked).  nibble_of turns it into visibility bits.
+__device__ __forceinline__ uint32_t mask_raw4(const uint8_t *row, int k, int Tk, bool vec4) {
+    if (vec4 && k + 3 < Tk) return *reinterpret_cast<const uint32_t *>(row + k);
+    uint32_t v = 0;
 #pragma unroll
     for (int e = 0; e < 4; e++)
-        if (k + e < Tk && row[k + e]) n |= 1u << e;
-    return n;
+        if (k + e < Tk && row[k + e]) v |= 0xffu << (8 * e);
+    return v;
+}
+// Visibility bits of keys [k, k+4) of one mask row.
+__device__ __forceinline__ uint32_t mask_nibble(const uint8_t *row, int k, int Tk, bool vec4) {
+    return nibble_of(mask_raw4(row, k, Tk, vec4));
+}
+// The 128 bits of a key tile from each lane's nibble (lane L holds keys
+// 4L .. 4L+3), gathered across the warp.
+__device__ __forceinline__ void nibbles_to_words(uint32_t nib, int lane, uint32_t w[4]) {
+    uint32_t word = nib << (4 * (lane & 7));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    w[0] = __shfl_sync(0xffffffffu, word, 0);
+    w[1] = __shfl_sync(0xffffffffu, word, 8);
+    w[2] = __shfl_sync(0xffffffffu, word, 16);
+    w[3] = __shfl_sync(0xffffffffu, word, 24);
 }
 
 // 128 visibility bits (4 words) of keys [key0, key0+128) for this thread's row.
@@ -368,15 +409,7 @@ __device__ __forceinline__ void mask_words(const TcParams &p, int b, int q_row, 
                                            uint32_t w[4]) {
     if (p.mask_kind == SP_MASK_KEY) {
         // warp-cooperative: lane covers keys key0 + 4*lane .. +3
-        const uint32_t nib = mask_nibble(p.mask, key0 + 4 * lane, p.Tk, p.mask_vec4);
-        uint32_t word = nib << (4 * (lane & 7));
-        word |= __shfl_xor_sync(0xffffffffu, word, 1);
-        word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        word |= __shfl_xor_sync(0xffffffffu, word, 4);
-        w[0] = __shfl_sync(0xffffffffu, word, 0);
-        w[1] = __shfl_sync(0xffffffffu, word, 8);
-        w[2] = __shfl_sync(0xffffffffu, word, 16);
-        w[3] = __shfl_sync(0xffffffffu, word, 24);
+        nibbles_to_words(mask_nibble(p.mask, key0 + 4 * lane, p.Tk, p.mask_vec4), lane, w);
         return;
     }
     if (p.mask_kind == SP_MASK_FULL && q_row < p.Tq) {
@@ -510,14 +543,7 @@ __device__ __forceinline__ void tail_words(const TcParams &p, int b, int q_row, 
             int s, row;
             if (tiling_tail(t, p.W, tt * 128 + 4 * lane + e, s, row) && p.mask[s * t.Tl + row]) nib |= 1u << e;
         }
-        uint32_t word = nib << (4 * (lane & 7));
-        word |= __shfl_xor_sync(0xffffffffu, word, 1);
-        word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        word |= __shfl_xor_sync(0xffffffffu, word, 4);
-        w[0] = __shfl_sync(0xffffffffu, word, 0);
-        w[1] = __shfl_sync(0xffffffffu, word, 8);
-        w[2] = __shfl_sync(0xffffffffu, word, 16);
-        w[3] = __shfl_sync(0xffffffffu, word, 24);
+        nibbles_to_words(nib, lane, w);
         return;
     }
     if (p.mask_kind == SP_MASK_FULL && q_row < p.Tq) {
@@ -557,6 +583,16 @@ __device__ __forceinline__ void key_words(const TcParams &p, int b, int q_row, i
     } else {
         tail_words(p, b, q_row, j - p.ktl.g0, lane, w);
     }
+}
+
+// key_words out of line, for the softmax loop of the sharded instance: there
+// the usual tile is a whole tile of unmasked keys, decided by one comparison,
+// and the rare others (partial and gathered tiles, masks) take this call, so
+// the loop's own code stays as small as the unsharded instance's.
+__device__ __noinline__ uint4 key_words_call(const TcParams &p, int b, int q_row, int j, int lane) {
+    uint32_t w[4];
+    key_words(p, b, q_row, j, lane, w);
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -873,9 +909,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // Visibility bits of the tile to come are fetched while the tensor core
         // still works on it, never between S arriving and P leaving.
         uint32_t w[4] = {0u, 0u, 0u, 0u};
+        // sharded K/V without a mask: key tiles below kfull are whole tiles of real keys
+        const int kfull = (TILED && p.ktl.sharded && p.mask_kind == SP_MASK_NONE) ? p.ktl.full0[p.W] : 0;
+        auto tiled_words = [&](int j) {
+            if (j < kfull) {
+                w[0] = w[1] = w[2] = w[3] = 0xffffffffu;
+            } else {
+                const uint4 v = key_words_call(p, b, q_row, j, lane);
+                w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+            }
+        };
+        // A key mask's bytes are loaded one tile before the tile whose bits
+        // they give, so that the shuffles that gather them never wait on the load.
+        const bool key_mask = !TILED && p.mask_kind == SP_MASK_KEY;
+        uint32_t raw_next = 0u;
         if (nkv > 0) {
-            if (TILED) key_words(p, b, q_row, key_tile(0), lane, w);
+            if (TILED) tiled_words(key_tile(0));
             else mask_words(p, b, q_row, key_tile(0) * 128, lane, w);
+            if (key_mask && nkv > 1) raw_next = mask_raw4(p.mask, key_tile(1) * 128 + 4 * lane, p.Tk, p.mask_vec4);
         }
         for (int jj = 0; jj < nkv; jj++) {
             const bool s_ok = wait_bounded(&bar_sf[i], (uint32_t)jj & 1u, abort_flag, p.status);
@@ -913,20 +964,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             l *= alpha;
             const float mc = (m == -INFINITY) ? 0.f : m * c;
             uint32_t pk[64];
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+            // packed pairs: s * c - m * c and the row-sum partials, two lanes
+            // per instruction (the same roundings as the scalar fmaf/add)
+            const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+            uint64_t l01 = 0ull, l23 = 0ull;
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-                const float p0 = ex2(fmaf(s[2 * e], c, -mc));
-                const float p1 = ex2(fmaf(s[2 * e + 1], c, -mc));
-                const float p2 = ex2(fmaf(s[2 * e + 2], c, -mc));
-                const float p3 = ex2(fmaf(s[2 * e + 3], c, -mc));
-                l0 += p0;
-                l1 += p1;
-                l2 += p2;
-                l3 += p3;
+                float x0, x1, x2, x3;
+                f2_unpack(f2_fma(f2_pack_u(sr[2 * e], sr[2 * e + 1]), c2, nmc2), x0, x1);
+                f2_unpack(f2_fma(f2_pack_u(sr[2 * e + 2], sr[2 * e + 3]), c2, nmc2), x2, x3);
+                const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+                l01 = f2_add(l01, f2_pack(p0, p1));
+                l23 = f2_add(l23, f2_pack(p2, p3));
                 pk[e] = pack_bf16x2(p0, p1);
                 pk[e + 1] = pack_bf16x2(p2, p3);
             }
+            float l0, l1, l2, l3;
+            f2_unpack(l01, l0, l1);
+            f2_unpack(l23, l2, l3);
             l += (l0 + l1) + (l2 + l3);
             tmem_st_x64(tS_me, pk);  // P over the first 64 columns of S_i
             // O_i already holds PV_i(jj-1) (see the issue order above); rescale
@@ -946,8 +1001,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             tc_fence_before();
             mbar_arrive(&bar_pf[i]);
             if (jj + 1 < nkv) {
-                if (TILED) key_words(p, b, q_row, key_tile(jj + 1), lane, w);
-                else mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
+                if (TILED) {
+                    tiled_words(key_tile(jj + 1));
+                } else if (key_mask) {
+                    nibbles_to_words(nibble_of(raw_next), lane, w);
+                    if (jj + 2 < nkv) raw_next = mask_raw4(p.mask, key_tile(jj + 2) * 128 + 4 * lane, p.Tk, p.mask_vec4);
+                } else {
+                    mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
+                }
             }
         }
         // the epilogue has a 128-thread barrier: the tile's four warps decide together
