@@ -340,7 +340,7 @@ def run_ours(args, world, rank, local):
     h2d = in_bytes + (um_host.numel() if um_host is not None else 0)
     d2h = out_host.numel() * out_host.element_size()
     with ClockSampler(dev.index) as clk_e2e:
-        e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev)
+        e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev, warmup=args.warmup)
     link = measure_link(host, out_host, dev)
     # ---- the same step through the fused exchange entry points (pad + tile +
     # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
@@ -482,13 +482,14 @@ def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> 
             "kernels_per_replay": per_step}
 
 
-def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev) -> float:
+def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev, warmup: int = 3) -> float:
     """Mean ms per step of `steps` end-to-end steps (H2D of every step's inputs,
-    the step, D2H of its output).  Two input and two output buffer sets, each
-    with the step captured once as a CUDA graph (SPStep.capture), so the host
-    issues one replay per step.  Uploads and downloads run on two copy streams
-    of their own: step i+1's uploads, step i's compute and step i-1's download
-    can all be in flight at once (ordered by events)."""
+    the step, D2H of its output), after `warmup` untimed runs of the same
+    pipeline.  Two input and two output buffer sets, each with the step
+    captured once as a CUDA graph (SPStep.capture), so the host issues one
+    replay per step.  Uploads and downloads run on two copy streams of their
+    own: step i+1's uploads, step i's compute and step i-1's download can all
+    be in flight at once (ordered by events)."""
     main = torch.cuda.current_stream(dev)
     up = torch.cuda.Stream(device=dev)
     down = torch.cuda.Stream(device=dev)
@@ -513,32 +514,38 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
                 d_um[slot].copy_(um_host, non_blocking=True)
             ev_in[slot].record(up)
 
+    def pipeline(n, t0, t1):
+        t0.record(main)
+        up.wait_event(t0)
+        down.wait_event(t0)
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                if i >= 1:
+                    up.wait_event(ev_done[1 - b])  # step i-1 is done with d_in[1-b]
+                upload(1 - b)
+            main.wait_event(ev_in[b])
+            if i >= 2:
+                main.wait_event(ev_d2h[b])  # step i-2's output has left d_out[b]
+            graphs[b].replay()
+            ev_done[b].record(main)
+            down.wait_event(ev_done[b])
+            with torch.cuda.stream(down):
+                out_pin[b].copy_(d_out[b], non_blocking=True)
+                ev_d2h[b].record(down)
+        main.wait_stream(up)
+        main.wait_stream(down)
+        t1.record(main)
+
+    torch.cuda.synchronize()
+    if warmup > 0:
+        pipeline(warmup, torch.cuda.Event(), torch.cuda.Event())
     barrier(world)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(main)
-    up.wait_event(t0)
-    down.wait_event(t0)
-    upload(0)
-    for i in range(steps):
-        b = i % 2
-        if i + 1 < steps:
-            if i >= 1:
-                up.wait_event(ev_done[1 - b])  # step i-1 is done with d_in[1-b]
-            upload(1 - b)
-        main.wait_event(ev_in[b])
-        if i >= 2:
-            main.wait_event(ev_d2h[b])  # step i-2's output has left d_out[b]
-        graphs[b].replay()
-        ev_done[b].record(main)
-        down.wait_event(ev_done[b])
-        with torch.cuda.stream(down):
-            out_pin[b].copy_(d_out[b], non_blocking=True)
-            ev_d2h[b].record(down)
-    main.wait_stream(up)
-    main.wait_stream(down)
-    t1.record(main)
+    pipeline(steps, t0, t1)
     torch.cuda.synchronize()
     barrier(world)
     del graphs
