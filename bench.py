@@ -44,6 +44,7 @@ METRIC = "masked-attn TFLOP/s + head-exchange GB/s per SP step, 1 GB300"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "c5"
 L2_FLUSH_BYTES = 512 << 20
+E2E_REPEATS = 3  # timed runs of the end-to-end loop; the line reports their median
 
 
 # ---------------------------------------------------------------- helpers
@@ -340,7 +341,9 @@ def run_ours(args, world, rank, local):
     h2d = in_bytes + (um_host.numel() if um_host is not None else 0)
     d2h = out_host.numel() * out_host.element_size()
     with ClockSampler(dev.index) as clk_e2e:
-        e2e_ms = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev, warmup=args.warmup)
+        e2e_runs = run_e2e_pipelined(step, host, um_host, out_host, args.steps, world, dev, warmup=args.warmup,
+                                     repeats=E2E_REPEATS)
+    e2e_ms = statistics.median(e2e_runs)
     link = measure_link(host, out_host, dev)
     # ---- the same step through the fused exchange entry points (pad + tile +
     # exchange in one pass per tensor; inverse exchange + gather + unpad in one)
@@ -380,6 +383,9 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "copies": "pinned host buffers on two copy streams; H2D of step i+1 and D2H of step i-1 overlap "
                           "step i's compute (the step replayed from a CUDA graph per buffer set)",
+                "runs_ms_per_step": [round(x, 4) for x in e2e_runs],
+                "timing": f"median of {E2E_REPEATS} timed runs of {args.steps} steps each, after "
+                          f"{args.warmup} warm-up steps of the same pipeline",
                 "link": link, "bound_ms_per_step": round(e2e_bound_ms, 4),
                 "frac_of_bound": round(e2e_bound_ms / e2e_ms, 4), "clocks": clk_e2e.summary()},
         "gpu_launches": launches,
@@ -482,10 +488,11 @@ def time_graph_step(step, d_in, d_um, args, world, flops, big_inputs, flush) -> 
             "kernels_per_replay": per_step}
 
 
-def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev, warmup: int = 3) -> float:
+def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev, warmup: int = 3,
+                      repeats: int = 1) -> list:
     """Mean ms per step of `steps` end-to-end steps (H2D of every step's inputs,
     the step, D2H of its output), after `warmup` untimed runs of the same
-    pipeline.  Two input and two output buffer sets, each with the step
+    pipeline; `repeats` timed runs of `steps` steps each, one figure per run.  Two input and two output buffer sets, each with the step
     captured once as a CUDA graph (SPStep.capture), so the host issues one
     replay per step.  Uploads and downloads run on two copy streams of their
     own: step i+1's uploads, step i's compute and step i-1's download can all
@@ -541,15 +548,18 @@ def run_e2e_pipelined(step, host, um_host, out_host, steps: int, world: int, dev
     torch.cuda.synchronize()
     if warmup > 0:
         pipeline(warmup, torch.cuda.Event(), torch.cuda.Event())
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    pipeline(steps, t0, t1)
-    torch.cuda.synchronize()
-    barrier(world)
+    runs = []
+    for _ in range(repeats):
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        pipeline(steps, t0, t1)
+        torch.cuda.synchronize()
+        barrier(world)
+        runs.append(max_over_ranks(t0.elapsed_time(t1) / steps, world))
     del graphs
-    return max_over_ranks(t0.elapsed_time(t1) / steps, world)
+    return runs
 
 
 def measure_link(host, out_host, dev, reps: int = 3) -> dict:
