@@ -322,9 +322,11 @@ SP_API int sp_attention(const void *const *q, const void *const *k, const void *
  *
  * Rank r's local head h is head r*Hl + h of every shard.  Its keys are
  * visited as every shard's whole 128-row tiles (loaded by TMA from the
- * shard), then "tail" tiles that gather the rows each shard has left,
- * n_s % 128 of them, copied row by row; queries are tiled the same way and
- * O rows go back to their shard.  Attention does not depend on the order of
+ * shard), then each shard's leftover block of n_s % 128 rows: by TMA as a
+ * partial tile when it holds at least 64 rows (the rows past the shard's end
+ * read as zeros and are masked), else packed with the other small leftover
+ * blocks into "gathered" tiles copied row by row; queries are tiled the same
+ * way and O rows go back to their shard.  Attention does not depend on the order of
  * its keys, so only the rounding of the key sum differs from sp_attention on
  * the exchanged (padded, key-masked) tensors; when Tl is a multiple of 128
  * the tiles are exactly the exchanged layout's and the result is the same
