@@ -341,7 +341,9 @@ SP_API int sp_attention(const void *const *q, const void *const *k, const void *
  * bf16 with D = 64 or 128 only (else SP_ERR_UNSUPPORTED), 16-byte aligned
  * pointers and strides (else SP_ERR_ALIGNMENT); Tk = 0 gives
  * SP_ERR_UNSUPPORTED.  Scale, workspace (sp_attention_workspace_bytes with
- * Hl = H/W and these Tq, Tk) and status as sp_attention. */
+ * Hl = H/W and these Tq, Tk) and status as sp_attention.  When the shards'
+ * leftover blocks add tiles (up to W more than ceil(T / 128)), a last wave
+ * that would want more split partials than that workspace holds runs whole. */
 #define SP_SHARD_KV 1
 #define SP_SHARD_Q 2
 SP_API int sp_attention_shards(const void *const *q, const void *const *k, const void *const *v, void *const *o,

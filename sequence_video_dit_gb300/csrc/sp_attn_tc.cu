@@ -1369,7 +1369,15 @@ int launch_attn_tc(const AttnArgs &a, cudaStream_t st) {
         prm.os[i] = a.os[i];
     }
     const bool tiled = a.q_shard_rows > 0 || a.kv_shard_rows > 0;
-    tc::SplitPlan sp = tc::plan_split(a.W, a.B, a.Tq, a.Tk, a.Hl, a.D, di.num_sms);
+    // Tiles of each operand.  A sharded one can have more than ceil(T / 128):
+    // every shard whose leftover block holds >= kPartialMin rows adds a partial
+    // tile of its own (up to W more in all), so the work decomposition counts
+    // the tiling's tiles, not the tokens.
+    auto n_tiles = [&](const tc::Tiling &t, int T) {
+        return t.sharded ? t.g0 + (t.tail0[a.W] + 127) / 128 : (T + 127) / 128;
+    };
+    const int q_tiles = n_tiles(prm.qtl, a.Tq), kv_tiles = n_tiles(prm.ktl, a.Tk);
+    tc::SplitPlan sp = tc::plan_split(a.W, a.B, q_tiles * 128, kv_tiles * 128, a.Hl, a.D, di.num_sms);
     if (sp.n_split > 1 && (a.extra == nullptr || a.extra_bytes < sp.extra_bytes)) {
         sp.n_split = 1;
         sp.kv_per_split = sp.n_kv > 0 ? sp.n_kv : 1;

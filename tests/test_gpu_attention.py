@@ -335,6 +335,46 @@ def test_attention_from_ragged_shards_matches_the_oracle(W, B, T, H, D, mask_kin
         assert max_abs(got[rows[:, 0], rows[:, 1], rows[:, 2]], ref) <= 2e-2
 
 
+def _random_ragged_shapes(n, seed=2024):
+    # W, B, T, H, D, mask_kind drawn once from a fixed generator: shard lengths
+    # ceil(T / W) with every mix of whole, partial (>= 64 leftover rows) and
+    # gathered (< 64) tiles, short and empty last shards
+    rng = np.random.default_rng(seed)
+    kinds = [sp.SP_MASK_NONE, sp.SP_MASK_KEY, sp.SP_MASK_FULL]
+    out = []
+    for _ in range(n):
+        W = int(rng.choice([2, 4, 8]))
+        out.append((W, int(rng.integers(1, 3)), int(rng.integers(1, 1500)), W * int(rng.integers(1, 3)),
+                    int(rng.choice([64, 128])), kinds[int(rng.integers(0, 3))]))
+    return out
+
+
+@pytest.mark.parametrize("W,B,T,H,D,mask_kind", _random_ragged_shapes(12))
+def test_attention_from_ragged_shards_random_shapes(W, B, T, H, D, mask_kind):
+    # The in-place attention on seeded random shapes, every row against the oracle.
+    g = torch.Generator().manual_seed(T * 13 + W * 3 + D)
+    q, k, v = (torch.randn(B, T, H, D, generator=g).bfloat16().cuda() for _ in range(3))
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = (torch.rand(T, generator=g) < 0.8).to(torch.uint8)
+        mask[0] = 1
+    elif mask_kind == sp.SP_MASK_FULL:
+        mask = (torch.rand(B, T, T, generator=g) < 0.4).to(torch.uint8)
+        for b in range(B):
+            mask[b, torch.arange(T), torch.arange(T)] = 1
+    Tl = -(-T // W)
+    views = lambda x: [x[:, min(s * Tl, T):min((s + 1) * Tl, T)] for s in range(W)]  # noqa: E731
+    out = torch.full((B, T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, H // W, D, torch.bfloat16))
+    sp.sp_attention_shards(views(q), views(k), views(v), views(out), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV,
+                           mask_kind, None if mask is None else mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    got = f32_np(out)
+    ref = oracle.attention(f32_np(q), f32_np(k), f32_np(v), mask_kind, None if mask is None else mask.numpy())
+    assert max_abs(got, ref) <= 2e-2
+
+
 @pytest.mark.parametrize("flags", [sp.SP_SHARD_KV, sp.SP_SHARD_Q])
 def test_ragged_shards_of_one_operand(flags):
     # Only K/V (the small-query cross-attention) or only Q (a small replicated
