@@ -128,3 +128,42 @@ def test_step_random_shapes(W, B, T, H, D, mask, variant):
         ref = oracle.attention(f32_np(q), f32_np(k), f32_np(v), oracle.MASK_FULL, um.numpy())
     assert out.shape == ref.shape
     assert max_abs(out, ref) <= BF16_TOL
+
+
+def _split_shape(rng):
+    # shapes that cut work items into key pieces: a short query (fewer items
+    # than SMs, >= 8 key tiles) or a long one whose last wave is partial
+    kind = KINDS[int(rng.integers(0, 3))]
+    D = int(rng.choice([64, 128]))
+    if rng.random() < 0.5:
+        W, Hl = int(rng.choice([1, 2, 4])), int(rng.integers(1, 3))
+        return (W, int(rng.integers(1, 3)), int(rng.integers(1, 400)), int(rng.integers(1024, 5000)), Hl, D, kind)
+    return (8, 1, int(rng.integers(2500, 5000)), int(rng.integers(1024, 3000)), 4, D, kind)
+
+
+@pytest.mark.parametrize("W,B,Tq,Tk,Hl,D,mask_kind", _shapes(15, 8, _split_shape))
+def test_split_attention_random_shapes(W, B, Tq, Tk, Hl, D, mask_kind):
+    g = torch.Generator().manual_seed(3 * Tq + Tk)
+    mk = lambda T: [torch.randn(B, T, Hl, D, generator=g).bfloat16().cuda() for _ in range(W)]  # noqa: E731
+    q, k, v = mk(Tq), mk(Tk), mk(Tk)
+    o = [torch.full_like(x, float("nan")) for x in q]
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = (torch.rand(Tk, generator=g) < 0.8).to(torch.uint8)
+        mask[0] = 1
+    elif mask_kind == sp.SP_MASK_FULL:
+        mask = (torch.rand(B, Tq, Tk, generator=g) < 0.3).to(torch.uint8)
+        mask[:, :, 0] = 1
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    sp.sp_attention(q, k, v, o, ws, mask_kind, None if mask is None else mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    rng = np.random.default_rng(Tq + Tk)
+    m_np = None if mask is None else mask.numpy()
+    for r in sorted({0, W - 1}):
+        qs = np.unique(np.concatenate([[0, Tq - 1], rng.integers(0, Tq, 24)]))
+        rows = np.array([(b, int(t), h) for b in range(B) for h in range(Hl) for t in qs], dtype=np.int64)
+        ref = oracle.attention_rows(f32_np(q[r]), f32_np(k[r]), f32_np(v[r]), rows, mask_kind, m_np)
+        got = f32_np(o[r])[rows[:, 0], rows[:, 1], rows[:, 2]]
+        assert np.isfinite(got).all()
+        assert max_abs(got, ref) <= BF16_TOL, f"rank {r}"
