@@ -167,3 +167,17 @@ def test_split_attention_random_shapes(W, B, Tq, Tk, Hl, D, mask_kind):
         got = f32_np(o[r])[rows[:, 0], rows[:, 1], rows[:, 2]]
         assert np.isfinite(got).all()
         assert max_abs(got, ref) <= BF16_TOL, f"rank {r}"
+
+
+def _grid_shape(rng):
+    # a latent grid the W-way split (the factor pair closest to a square) divides
+    W = int(rng.choice([1, 2, 3, 4, 6, 8]))
+    sh, sw = oracle.optimal_split(W)
+    grid = (int(rng.integers(1, 5)), sh * int(rng.integers(1, 7)), sw * int(rng.integers(1, 7)))
+    dtype = [torch.float32, torch.bfloat16][int(rng.integers(0, 2))]
+    return (int(rng.integers(1, 3)), grid, W, W * int(rng.integers(1, 3)), int(rng.choice([4, 8, 16, 64])), dtype)
+
+
+@pytest.mark.parametrize("B,grid,W,H,D,dtype", _shapes(16, 8, _grid_shape))
+def test_2d_split_random_shapes(B, grid, W, H, D, dtype):
+    layout_tests.test_tile_2d_and_gather_2d_bit_exact(B, grid, W, H, D, dtype)
