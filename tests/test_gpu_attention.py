@@ -68,6 +68,34 @@ def test_cuda_core_attention(W, B, Tq, Tk, Hl, D, dtype, mask_kind):
     _run(W, B, Tq, Tk, Hl, D, dtype, mask_kind)
 
 
+def test_misaligned_buffers_take_the_cuda_core_kernel():
+    # bf16, D = 128, but every tensor starts 2 bytes past a 16-byte boundary:
+    # TMA cannot address them, so the call runs on the CUDA-core kernel and
+    # must still match the oracle
+    W, B, T, Hl, D = 2, 1, 300, 2, 128
+    g = torch.Generator().manual_seed(77)
+    n = B * T * Hl * D
+
+    def off(x):
+        buf = torch.empty(n + 1, dtype=torch.bfloat16, device="cuda")
+        view = buf[1:].view(B, T, Hl, D)
+        view.copy_(x)
+        return view
+
+    q, k, v = ([off(t.cuda()) for t in _mk(W, B, T, Hl, D, torch.bfloat16, g)] for _ in range(3))
+    o = [off(torch.full((B, T, Hl, D), float("nan"), dtype=torch.bfloat16)) for _ in range(W)]
+    assert all(x.data_ptr() % 16 == 2 for x in q + k + v + o)
+    mask = (torch.rand(T, generator=g) < 0.8).to(torch.uint8)
+    mask[0] = 1
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, Hl, D, torch.bfloat16))
+    sp.sp_attention(q, k, v, o, ws, sp.SP_MASK_KEY, mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    for r in range(W):
+        ref = oracle.attention(f32_np(q[r]), f32_np(k[r]), f32_np(v[r]), oracle.MASK_KEY, mask.numpy())
+        assert max_abs(f32_np(o[r]), ref) <= 2e-2, f"rank {r}"
+
+
 def test_large_logits_rescale():
     # Scores spread over a wide range force the running max to move by more
     # than the lazy-rescale threshold many times.
