@@ -599,7 +599,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     constexpr int NSLOT = C::NSLOT;  // ring slots
     constexpr int SLOT = C::TILE;    // bytes per slot
     extern __shared__ uint8_t dsm_raw[];
-    __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_empty[NSLOT];
+    // Ring slots are freed by release events, one tcgen05.commit each: event
+    // 0 (after QK1(0)) frees K(0); event e >= 1 (after QK1(e), issued in step
+    // e-1, which also orders PV1(e-1) before it) frees V(e-1) and K(e), the
+    // loads 2e-1 and 2e.  So load m is free after event ceil(m / 2).  Events
+    // go round NREL barriers: while the producer waits for event e before
+    // its load n = m + NSLOT, at most n - 1 <= 2e + NSLOT - 1 loads exist, and
+    // event e + NREL needs load 2(e + NREL) > that, so a barrier never runs a
+    // whole phase past the one its waiter expects.
+    constexpr int NREL = NSLOT / 2 + 1;
+    __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_rel[NREL];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -661,7 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         mbar_init(&bar_q, 1);
         for (int s = 0; s < NSLOT; s++) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1);
+        }
+        for (int s = 0; s < NREL; s++) {
+            mbar_init(&bar_rel[s], 1);
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar_sf[i], 1);
@@ -702,8 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (; n < nloads; n++) {
                 const int slot = n % NSLOT;
                 const int use = n / NSLOT;
-                if (use > 0 && !wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status))
-                    break;
+                if (use > 0) {  // the slot's previous load (n - NSLOT) has been consumed
+                    const int e = (n - NSLOT + 1) >> 1;
+                    if (!wait_bounded(&bar_rel[e % NREL], (uint32_t)(e / NREL) & 1u, abort_flag, p.status)) break;
+                }
                 mbar_arrive_expect_tx(&bar_full[slot], SLOT);
                 const CUtensorMap *m = (n & 1) ? &p.tv[r] : &p.tk[r];
                 const int krow = key_tile(n >> 1) * 128;
@@ -759,7 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const int use = n / NSLOT;
                 bool ok = true;
                 if (use > 0 && lane == 0)
-                    ok = wait_bounded(&bar_empty[slot], (uint32_t)(use - 1) & 1u, abort_flag, p.status);
+                    ok = wait_bounded(&bar_rel[((n - NSLOT + 1) >> 1) % NREL],
+                                      (uint32_t)(((n - NSLOT + 1) >> 1) / NREL) & 1u, abort_flag, p.status);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
                 const int j = key_tile(n >> 1);
                 if (!p.ktl.sharded || j < p.ktl.g0) {
@@ -834,7 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
             auto kslot = [](int j) { return (2 * j) % NSLOT; };
             // a slot is free once the MMAs that read it have completed
-            auto release = [&](int slot) { mma_commit(&bar_empty[slot]); };
+            // release event e (see bar_rel)
+            auto release = [&](int e) { mma_commit(&bar_rel[e % NREL]); };
             auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };
             auto kpar = [](int j) { return (uint32_t)((2 * j) / NSLOT) & 1u; };
             auto vpar = [](int j) { return (uint32_t)((2 * j + 1) / NSLOT) & 1u; };
@@ -850,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 signal(&bar_sf[0]);
                 qk(1, kslot(0));
                 signal(&bar_sf[1]);
-                release(kslot(0));
+                release(0);
             }
             for (int jj = 0; ok && jj < nkv; jj++) {
                 const bool more = jj + 1 < nkv;
@@ -869,11 +884,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (!p_ready(1, (uint32_t)jj & 1u)) break;
                 tc_fence_after();
                 pv(1, vslot(jj), jj > 0);
-                release(vslot(jj));
                 if (more) {
                     qk(1, kslot(jj + 1));
                     signal(&bar_sf[1]);
-                    release(kslot(jj + 1));
+                    release(jj + 1);  // V(jj) and K(jj+1)
                 } else {
                     signal(&bar_of[1]);
                 }
