@@ -608,6 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // event e + NREL needs load 2(e + NREL) > that, so a barrier never runs a
     // whole phase past the one its waiter expects.
     constexpr int NREL = NSLOT / 2 + 1;
+    // Who signals the release events: the per-rank instance lets the first
+    // lane of tile 1's first softmax warp relay each one with a plain arrive
+    // as soon as it sees S1 ready (the same completion point, one commit per
+    // step fewer); the sharded instance commits them from the MMA thread
+    // (it measured faster that way).
+    constexpr bool RELAY = !TILED;
     __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_rel[NREL];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
@@ -848,8 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
             auto kslot = [](int j) { return (2 * j) % NSLOT; };
             // a slot is free once the MMAs that read it have completed
-            // release event e (see bar_rel)
-            auto release = [&](int e) { mma_commit(&bar_rel[e % NREL]); };
+            // release event e (see bar_rel), when the MMA thread signals it
+            auto release = [&](int e) {
+                if constexpr (!RELAY) mma_commit(&bar_rel[e % NREL]);
+            };
             auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };
             auto kpar = [](int j) { return (uint32_t)((2 * j) / NSLOT) & 1u; };
             auto vpar = [](int j) { return (uint32_t)((2 * j + 1) / NSLOT) & 1u; };
@@ -943,6 +951,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 ok = false;
                 break;
             }
+            // S1(jj) complete means QK1(jj) and every MMA before it (PV1(jj-1))
+            // have completed: relay release event jj (frees V(jj-1) and K(jj))
+            if (RELAY && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld_x128(tS_me, sr);
