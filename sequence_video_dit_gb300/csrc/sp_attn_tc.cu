@@ -607,13 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // its load n = m + NSLOT, at most n - 1 <= 2e + NSLOT - 1 loads exist, and
     // event e + NREL needs load 2(e + NREL) > that, so a barrier never runs a
     // whole phase past the one its waiter expects.
+    // No tcgen05.commit signals them: the S1(j) commit already marks event j's
+    // completion point, so the first lane of tile 1's first softmax warp,
+    // which waits for it anyway, relays event j with a plain arrive at the
+    // end of its iteration j.
     constexpr int NREL = NSLOT / 2 + 1;
-    // Who signals the release events: the per-rank instance lets the first
-    // lane of tile 1's first softmax warp relay each one with a plain arrive
-    // as soon as it sees S1 ready (the same completion point, one commit per
-    // step fewer); the sharded instance commits them from the MMA thread
-    // (it measured faster that way).
-    constexpr bool RELAY = !TILED;
     __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_rel[NREL];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
@@ -854,10 +852,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             // K of key tile j sits in slot (2j) % NSLOT, V in slot (2j+1) % NSLOT
             auto kslot = [](int j) { return (2 * j) % NSLOT; };
             // a slot is free once the MMAs that read it have completed
-            // release event e (see bar_rel), when the MMA thread signals it
-            auto release = [&](int e) {
-                if constexpr (!RELAY) mma_commit(&bar_rel[e % NREL]);
-            };
             auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };
             auto kpar = [](int j) { return (uint32_t)((2 * j) / NSLOT) & 1u; };
             auto vpar = [](int j) { return (uint32_t)((2 * j + 1) / NSLOT) & 1u; };
@@ -873,7 +867,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 signal(&bar_sf[0]);
                 qk(1, kslot(0));
                 signal(&bar_sf[1]);
-                release(0);
             }
             for (int jj = 0; ok && jj < nkv; jj++) {
                 const bool more = jj + 1 < nkv;
@@ -895,7 +888,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (more) {
                     qk(1, kslot(jj + 1));
                     signal(&bar_sf[1]);
-                    release(jj + 1);  // V(jj) and K(jj+1)
                 } else {
                     signal(&bar_of[1]);
                 }
@@ -951,9 +943,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 ok = false;
                 break;
             }
-            // S1(jj) complete means QK1(jj) and every MMA before it (PV1(jj-1))
-            // have completed: relay release event jj (frees V(jj-1) and K(jj))
-            if (RELAY && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld_x128(tS_me, sr);
@@ -1030,6 +1019,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     mask_words(p, b, q_row, key_tile(jj + 1) * 128, lane, w);
                 }
             }
+            // S1(jj) was complete, so QK1(jj) and every MMA before it
+            // (PV1(jj-1)) have completed: release event jj frees V(jj-1), K(jj)
+            if (i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
         }
         // the epilogue has a 128-thread barrier: the tile's four warps decide together
         const bool epi = named_bar_and(1 + i, 128, ok && !*abort_flag);
