@@ -362,6 +362,11 @@ __device__ __forceinline__ uint64_t f2_pack_u(uint32_t lo, uint32_t hi) {
 __device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -979,24 +984,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             l *= alpha;
             const float mc = (m == -INFINITY) ? 0.f : m * c;
             uint32_t pk[64];
-            // s * c - m * c on packed pairs, two lanes per instruction (the same
-            // rounding as the scalar fmaf).  The row-sum partials stay scalar:
-            // packing them too ties up register pairs and spills in this loop.
+            // s * c - m * c and the four row-sum partials on packed pairs, two
+            // lanes per instruction (each lane rounds as the scalar fmaf / fadd)
             const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+            uint64_t l01 = 0ull, l23 = 0ull;  // packed partial sums, lanes (0,1) and (2,3)
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
                 float x0, x1, x2, x3;
                 f2_unpack(f2_fma(f2_pack_u(sr[2 * e], sr[2 * e + 1]), c2, nmc2), x0, x1);
                 f2_unpack(f2_fma(f2_pack_u(sr[2 * e + 2], sr[2 * e + 3]), c2, nmc2), x2, x3);
                 const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-                l0 += p0;
-                l1 += p1;
-                l2 += p2;
-                l3 += p3;
+                l01 = f2_add(l01, f2_pack(p0, p1));
+                l23 = f2_add(l23, f2_pack(p2, p3));
                 pk[e] = pack_bf16x2(p0, p1);
                 pk[e + 1] = pack_bf16x2(p2, p3);
             }
+            float l0, l1, l2, l3;
+            f2_unpack(l01, l0, l1);
+            f2_unpack(l23, l2, l3);
             l += (l0 + l1) + (l2 + l3);
             tmem_st_x64(tS_me, pk);  // P over the first 64 columns of S_i
             // O_i already holds PV_i(jj-1) (see the issue order above); rescale
