@@ -617,8 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // whole phase past the one its waiter expects.
     // No tcgen05.commit signals them: the S1(j) commit already marks event j's
     // completion point, so the first lane of tile 1's first softmax warp,
-    // which waits for it anyway, relays event j with a plain arrive at the
-    // end of its iteration j.
+    // which waits for it anyway, relays event j with a plain arrive: at the
+    // end of its iteration j, or, in the sharded instance, as soon as S1(j)
+    // is in registers (each place measured fastest for its instance).
     constexpr int NREL = NSLOT / 2 + 1;
     __shared__ __align__(8) uint64_t bar_q, bar_full[NSLOT], bar_rel[NREL];
     __shared__ __align__(8) uint64_t bar_sf[2], bar_pf[2], bar_of[2], bar_drain;
@@ -955,6 +956,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             uint32_t sr[128];
             float mt;  // the row's maximum, reduced by the TMEM load itself
             tmem_ld_max_x128(tS_me, sr, mt);
+            // the sharded instance relays release event jj as soon as S1(jj) is in
+            if (TILED && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
             float *s = reinterpret_cast<float *>(sr);
             if ((w[0] & w[1] & w[2] & w[3]) != 0xffffffffu) {
                 // some keys of the tile are hidden: mask them, then the maximum
@@ -1032,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             // S1(jj) was complete, so QK1(jj) and every MMA before it
             // (PV1(jj-1)) have completed: release event jj frees V(jj-1), K(jj)
-            if (i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
+            if (!TILED && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);
         }
         // the epilogue has a 128-thread barrier: the tile's four warps decide together
         const bool epi = named_bar_and(1 + i, 128, ok && !*abort_flag);

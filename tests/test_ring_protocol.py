@@ -3,16 +3,18 @@
 The kernel's producer warp streams K and V tiles through NSLOT shared-memory
 slots in the order K0 V0 K1 V1 ... (load n goes to slot n % NSLOT).  A slot
 is reused once the MMAs that read its previous load have completed, which the
-kernel learns from release events: event e is relayed by tile 1's softmax at
-the end of its iteration e, after it saw the commit that follows QK1(e), so
-every MMA issued before that commit has completed.  The producer waits for
+kernel learns from release events: event e is relayed by tile 1's softmax
+once it saw the commit that follows QK1(e), so every MMA issued before that
+commit has completed.  The per-rank instance relays it at the end of the
+softmax iteration, after P1(e) is handed over; the sharded instance relays it
+as soon as S1(e) is loaded, before P1(e).  The producer waits for
 event (n - NSLOT + 1) >> 1 before load n >= NSLOT, on barrier e % NREL with
 parity (e // NREL) & 1, NREL = NSLOT // 2 + 1.
 
 The model runs the roles (producer, MMA issuer, the two softmax tiles) as
 sequential programs.  Tensor-core work completes as late as the protocol
 allows: a commit fires only when no role can otherwise progress.  It checks,
-for every key-tile count up to 64 and both ring sizes, that
+for every key-tile count up to 64, both ring sizes and both relay places, that
 - every role finishes (no wait that never ends),
 - no load overwrites a slot whose previous load still has an MMA in flight,
 - no release barrier runs a whole phase past the one its waiter expects.
@@ -46,7 +48,8 @@ def test_model_matches_the_kernel_source():
     assert "wait_bounded(&bar_rel[e % NREL], (uint32_t)(e / NREL) & 1u" in src
     assert "auto kslot = [](int j) { return (2 * j) % NSLOT; };" in src
     assert "auto vslot = [](int j) { return (2 * j + 1) % NSLOT; };" in src
-    assert "if (i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);" in src
+    assert "if (!TILED && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);" in src
+    assert "if (TILED && i == 1 && quarter == 0 && lane == 0) mbar_arrive(&bar_rel[jj % NREL]);" in src
 
 
 def _mma_program(nkv):
@@ -65,9 +68,11 @@ def _mma_program(nkv):
     return prog
 
 
-def _run(nkv, nslot, early=0):
+def _run(nkv, nslot, early=0, relay_on_load=False):
     """Runs the protocol to its end; `early` > 0 makes the producer wait for
-    an event that many steps too early (a broken variant)."""
+    an event that many steps too early (a broken variant).  relay_on_load:
+    tile 1 relays event j when S1(j) arrives and hands P1(j) over only when
+    no other role can move (as late as possible)."""
     nrel = nslot // 2 + 1
     n_loads = 2 * nkv
     landed = set()
@@ -82,6 +87,7 @@ def _run(nkv, nslot, early=0):
     n = 0                        # producer: next load
     mi = 0                       # MMA issuer: next op
     sm = {0: 0, 1: 0}            # softmax tile i: next iteration
+    held = False                 # relay_on_load: tile 1 relayed its event, P1 not handed over yet
     prog = _mma_program(nkv)
     while True:
         moved = False
@@ -117,13 +123,23 @@ def _run(nkv, nslot, early=0):
             mi += 1
             moved = True
         for i in (0, 1):         # softmax: S_i(j) in, P_i(j) out; tile 1 relays event j
-            while sm[i] < nkv and fired[("sf", i)] > sm[i]:
+            while sm[i] < nkv and fired[("sf", i)] > sm[i] and not (i == 1 and held):
+                if i == 1 and relay_on_load:
+                    events += 1
+                    held = True
+                    moved = True
+                    break
                 p_ready[i] += 1
                 if i == 1:
                     events += 1
                 sm[i] += 1
                 moved = True
         if moved:
+            continue
+        if held:                 # nothing else can move: tile 1 hands P1 over
+            held = False
+            p_ready[1] += 1
+            sm[1] += 1
             continue
         if not pending:
             break
@@ -137,16 +153,18 @@ def _run(nkv, nslot, early=0):
     assert fired[("of", 0)] == 1 and fired[("of", 1)] == 1
 
 
+@pytest.mark.parametrize("relay_on_load", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
-def test_ring_protocol_finishes_and_never_overwrites_a_slot_in_use(D):
+def test_ring_protocol_finishes_and_never_overwrites_a_slot_in_use(D, relay_on_load):
     nslot = _ring_sizes()[D]
     for nkv in range(1, 65):
-        _run(nkv, nslot)
+        _run(nkv, nslot, relay_on_load=relay_on_load)
 
 
+@pytest.mark.parametrize("relay_on_load", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
-def test_the_model_catches_a_release_one_event_early(D):
+def test_the_model_catches_a_release_one_event_early(D, relay_on_load):
     nslot = _ring_sizes()[D]
     with pytest.raises(AssertionError, match="in use"):
         for nkv in range(1, 65):
-            _run(nkv, nslot, early=1)
+            _run(nkv, nslot, early=1, relay_on_load=relay_on_load)
