@@ -470,3 +470,91 @@ def test_concurrent_host_threads_give_the_same_bytes():
         assert st == 0
         for a, b in zip(o, ref):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# The row maximum of a key tile comes from the TMEM load of S itself; a tile
+# with hidden keys must recompute it over the visible ones.  These inputs make
+# the hidden keys (masked, or past the end of the keys) the largest scores of
+# every row: every query is +3, a visible key -3, a hidden key +3, so the
+# scores are -9 D and +9 D (zero for keys the tile loads past the end).  A
+# maximum taken over hidden keys would flush every visible probability to
+# zero; the right answer is the plain mean of the visible V rows.
+def _hidden_max_inputs(B, Tq, Tk, H, D, hidden, g):
+    q = torch.full((B, Tq, H, D), 3.0).bfloat16()
+    k = torch.full((B, Tk, H, D), -3.0)
+    if len(hidden):
+        k[:, hidden] = 3.0
+    v = torch.randn(B, Tk, H, D, generator=g).bfloat16()
+    return q, k.bfloat16(), v
+
+
+def _mean_of_visible(v, visible, Tq):
+    # closed form: uniform softmax over the visible keys, for every query
+    m = f32_np(v)[:, visible].astype(np.float64).mean(axis=1, keepdims=True)
+    return np.repeat(m, Tq, axis=1)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask_kind", [sp.SP_MASK_KEY, sp.SP_MASK_FULL])
+def test_hidden_keys_with_the_largest_scores_leave_the_row_max(mask_kind, D):
+    W, B, Tq, Tk, Hl = 2, 1, 256, 300, 2
+    hidden = [5, 77, 130, 200, 201, 202, 299]
+    visible = [t for t in range(Tk) if t not in hidden]
+    g = torch.Generator().manual_seed(41 + D)
+    ranks = [_hidden_max_inputs(B, Tq, Tk, Hl, D, hidden, g) for _ in range(W)]
+    keep = torch.ones(Tk, dtype=torch.uint8)
+    keep[hidden] = 0
+    mask = keep if mask_kind == sp.SP_MASK_KEY else keep.view(1, 1, Tk).repeat(B, Tq, 1).contiguous()
+    q, k, v = ([x[i].cuda() for x in ranks] for i in range(3))
+    o = [torch.full_like(x, float("nan")) for x in q]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    sp.sp_attention(q, k, v, o, ws, mask_kind, mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    for r in range(W):
+        got = f32_np(o[r])
+        assert np.isfinite(got).all()
+        assert max_abs(got, _mean_of_visible(ranks[r][2], visible, Tq)) <= 2e-2
+        ref = oracle.attention(f32_np(ranks[r][0]), f32_np(ranks[r][1]), f32_np(ranks[r][2]), mask_kind, mask.numpy())
+        assert max_abs(got, ref) <= 2e-2
+
+
+def test_keys_past_the_end_leave_the_row_max():
+    # no mask, 300 keys: the last key tile's columns past key 299 hold zeros
+    # (the load fills them), larger than every real score (-1152)
+    W, B, Tq, Tk, Hl, D = 1, 1, 256, 300, 2, 128
+    g = torch.Generator().manual_seed(43)
+    q, k, v = _hidden_max_inputs(B, Tq, Tk, Hl, D, [], g)
+    o = [torch.full_like(q, float("nan")).cuda()]
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, Tq, Tk, Hl, D, torch.bfloat16))
+    sp.sp_attention([q.cuda()], [k.cuda()], [v.cuda()], o, ws)
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    got = f32_np(o[0])
+    assert max_abs(got, _mean_of_visible(v, list(range(Tk)), Tq)) <= 2e-2
+
+
+@pytest.mark.parametrize("mask_kind", [sp.SP_MASK_NONE, sp.SP_MASK_KEY])
+def test_sharded_tiles_with_hidden_keys_leave_the_row_max(mask_kind):
+    # The exchange inside the attention, ragged shards (partial and gathered
+    # key tiles whose rows past a shard's end hold zeros or stale keys).
+    W, B, T, H, D = 4, 1, 771, 8, 128
+    hidden = [3, 190, 194, 400, 770] if mask_kind == sp.SP_MASK_KEY else []
+    visible = [t for t in range(T) if t not in hidden]
+    g = torch.Generator().manual_seed(44)
+    q, k, v = (x.cuda() for x in _hidden_max_inputs(B, T, T, H, D, hidden, g))
+    mask = None
+    if mask_kind == sp.SP_MASK_KEY:
+        mask = torch.ones(T, dtype=torch.uint8)
+        mask[hidden] = 0
+    Tl = -(-T // W)
+    views = lambda x: [x[:, min(s * Tl, T):min((s + 1) * Tl, T)] for s in range(W)]  # noqa: E731
+    out = torch.full((B, T, H, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = sp.new_workspace(sp.sp_attention_workspace_bytes(W, B, T, T, H // W, D, torch.bfloat16))
+    sp.sp_attention_shards(views(q), views(k), views(v), views(out), ws, sp.SP_SHARD_Q | sp.SP_SHARD_KV,
+                           mask_kind, None if mask is None else mask.cuda())
+    torch.cuda.synchronize()
+    assert sp.sp_workspace_status(ws)[0] == 0
+    got = f32_np(out)
+    assert np.isfinite(got).all()
+    assert max_abs(got, _mean_of_visible(v.cpu(), visible, T)) <= 2e-2
